@@ -1,0 +1,72 @@
+// KV commit (K7): the accepted path's K/V rows join the cache.
+//
+// Ultralytics glossary "Medusa Heads", section "Tree attention and accepting
+// tokens": the longest branch the model accepts is kept; wiblog.cn "Medusa
+// multi-head speculative decoding", section "Inference flow in an online chat
+// service": the accepted tokens are emitted and the next round starts from the
+// last of them.  The tree pass already computed the K/V rows of every node, so
+// keeping a branch means copying the rows of its nodes (depth 0..a) to cache
+// positions kv_len..kv_len+a.  One CTA per request: it reads kv_len once,
+// copies with 16-byte vectors and only then publishes the new length.
+#include "tree.cuh"
+
+using namespace medusa;
+
+namespace {
+
+__global__ void __launch_bounds__(256) kv_commit_kernel(medusa_tree_dev tr, const uint4* __restrict__ k_new,
+                                                        const uint4* __restrict__ v_new, uint4* __restrict__ k_cache,
+                                                        uint4* __restrict__ v_cache, int32_t* __restrict__ kv_len,
+                                                        const int32_t* __restrict__ best_node, int Hkv, int row_vecs,
+                                                        int Lmax, int32_t* __restrict__ dev_status) {
+  __shared__ int chain[MEDUSA_MAX_DEPTH + 1];
+  __shared__ int s_n, s_L;
+  const int b = blockIdx.x;
+  const int T = tr.T;
+  if (threadIdx.x == 0) {
+    int best = best_node[b];
+    if (best < 0 || best >= T) best = 0;
+    const int a = tr.depth[best];
+    for (int n = best; n >= 0; n = tr.parent[n]) chain[tr.depth[n]] = n;
+    const int L = kv_len[b];
+    s_L = L;
+    s_n = (L < 0 || L + a + 1 > Lmax) ? -1 : a + 1;
+    if (s_n < 0 && dev_status) atomicOr(dev_status + b, MEDUSA_DEV_KV_OVERFLOW);
+  }
+  __syncthreads();
+  const int n = s_n, L = s_L;
+  if (n < 0) return;
+  // element e -> (depth d, kv head g, 16-byte vector j of a row)
+  const int per_d = Hkv * row_vecs;
+  for (int e = threadIdx.x; e < n * per_d; e += blockDim.x) {
+    const int d = e / per_d, g = (e / row_vecs) % Hkv, j = e % row_vecs;
+    const size_t src = ((static_cast<size_t>(b) * T + chain[d]) * Hkv + g) * row_vecs + j;
+    const size_t dst = ((static_cast<size_t>(b) * Hkv + g) * Lmax + L + d) * row_vecs + j;
+    k_cache[dst] = k_new[src];
+    v_cache[dst] = v_new[src];
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) kv_len[b] = L + n;
+}
+
+}  // namespace
+
+MEDUSA_API int medusa_kv_commit(const medusa_tree* tree, const void* k_new, const void* v_new, void* k_cache,
+                                void* v_cache, int32_t* kv_len, const int32_t* best_node, int32_t B, int32_t Hkv,
+                                int32_t D, int32_t Lmax, medusa_dtype dtype, int32_t* dev_status,
+                                medusa_stream_t stream) {
+  if (!tree || !k_new || !v_new || !k_cache || !v_cache || !kv_len || !best_node) return MEDUSA_ERR_INVALID_ARG;
+  if (B < 1 || B > MEDUSA_MAX_BATCH || Hkv < 1 || D < 1 || Lmax < 0) return MEDUSA_ERR_INVALID_ARG;
+  if (dtype != MEDUSA_F32 && dtype != MEDUSA_BF16) return MEDUSA_ERR_INVALID_ARG;
+  const int es = dtype == MEDUSA_BF16 ? 2 : 4;
+  if ((D * es) % 16 != 0) return MEDUSA_ERR_UNSUPPORTED;
+  const void* ptrs[] = {k_new, v_new, k_cache, v_cache, kv_len, best_node};
+  for (const void* q : ptrs)
+    if (!aligned16(q)) return MEDUSA_ERR_ALIGNMENT;
+  if (dev_status && !aligned16(dev_status)) return MEDUSA_ERR_ALIGNMENT;
+  kv_commit_kernel<<<B, 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+      tree->dev, static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new), static_cast<uint4*>(k_cache),
+      static_cast<uint4*>(v_cache), kv_len, best_node, Hkv, D * es / 16, Lmax, dev_status);
+  MEDUSA_LAUNCH_CHECK();
+  return MEDUSA_OK;
+}

@@ -1,0 +1,109 @@
+// Shared device helpers of the Medusa step kernels (sm_103a).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <cfloat>
+
+#include "../../include/medusa.h"
+
+#define MEDUSA_API extern "C" __attribute__((visibility("default")))
+
+namespace medusa {
+
+constexpr int kWarp = 32;
+
+__host__ __device__ inline int cdiv(int a, int b) { return (a + b - 1) / b; }
+__host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+// --------------------------------------------------------------------------
+// Element access for the two storage types
+// --------------------------------------------------------------------------
+template <typename T> struct Elem;
+template <> struct Elem<float> {
+  static constexpr int kPer16B = 4;
+  __device__ static inline float to_f(float x) { return x; }
+  __device__ static inline float from_f(float x) { return x; }
+};
+template <> struct Elem<__nv_bfloat16> {
+  static constexpr int kPer16B = 8;
+  __device__ static inline float to_f(__nv_bfloat16 x) { return __bfloat162float(x); }
+  __device__ static inline __nv_bfloat16 from_f(float x) { return __float2bfloat16_rn(x); }
+};
+
+// 16-byte streaming load that does not allocate in L1 (weights are read once).
+__device__ inline uint4 ld_stream16(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
+
+// Unpack 16 bytes into fp32 values.
+__device__ inline void unpack16(const uint4& v, float (&f)[8], __nv_bfloat16*) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[2 * i] = __uint_as_float(w[i] << 16);
+    f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+  }
+}
+__device__ inline void unpack16(const uint4& v, float (&f)[4], float*) {
+  f[0] = __uint_as_float(v.x);
+  f[1] = __uint_as_float(v.y);
+  f[2] = __uint_as_float(v.z);
+  f[3] = __uint_as_float(v.w);
+}
+
+// --------------------------------------------------------------------------
+// Warp reductions
+// --------------------------------------------------------------------------
+__device__ inline float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// (value, id) ordering used by every top-k / argmax: larger value first, equal
+// values by lower id; NaN is never "better" than anything.
+__device__ inline bool better(float va, int ia, float vb, int ib) {
+  return (va > vb) || (va == vb && ia < ib);
+}
+
+__device__ inline void warp_argmax(float& v, int& id) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    float ov = __shfl_xor_sync(0xffffffffu, v, o);
+    int oi = __shfl_xor_sync(0xffffffffu, id, o);
+    if (better(ov, oi, v, id)) { v = ov; id = oi; }
+  }
+}
+
+__device__ inline uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ inline uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Bounded-wait limit for every device-side spin (about one second).
+constexpr uint64_t kSpinLimitNs = 1000000000ull;
+
+}  // namespace medusa
+
+// Host-side launch error check used by every entry point.
+#define MEDUSA_LAUNCH_CHECK()                                  \
+  do {                                                         \
+    if (cudaPeekAtLastError() != cudaSuccess) {                \
+      (void)cudaGetLastError();                                \
+      return MEDUSA_ERR_CUDA;                                  \
+    }                                                          \
+  } while (0)

@@ -1,0 +1,283 @@
+// Medusa heads (K1 + K2): u_k = h + SiLU(W1_k h + b1_k), z_k = W2_k u_k, per-head top-k.
+//
+// Ultralytics glossary "Medusa Heads", section "How the heads predict the next
+// tokens": each head is one fully connected layer with SiLU and a residual
+// connection followed by a bias-free projection onto the vocabulary, and every
+// head reads the same last hidden state.  wiblog.cn "Medusa multi-head
+// speculative decoding", section "Medusa decoding heads": each head outputs
+// its top-k candidates.
+//
+// Both launches are HBM streams of weight rows (the batch has few rows, so
+// the dot products run on CUDA cores from a shared-memory copy of the
+// activations).  K2 fuses the top-k: every CTA keeps the top-k of its slice of
+// the vocabulary, and the last CTA of a head (ticket counter) merges them.
+#include <algorithm>
+
+#include "gemv.cuh"
+
+using namespace medusa;
+
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+constexpr int kRows = 4;  // weight rows per warp pass
+constexpr int kTargetCtas = 148 * 4;
+constexpr size_t kMaxXBytes = 96 * 1024;  // activation rows staged per launch
+
+template <int BMAX> struct Unroll { static constexpr int U = BMAX <= 2 ? 4 : 2; };
+
+struct HeadsPlan {
+  int nblk;     // K heads (+1 for the lm_head root block)
+  int groups;   // row groups of kRows per warp
+  int rpc;      // rows per CTA
+  int cph;      // CTAs per block (head)
+  int bgroup;   // batch rows per launch
+  int fc_groups;
+  int fc_ctas;
+};
+
+HeadsPlan plan_heads(int B, int H, int V, int K, int with_root, int esize) {
+  HeadsPlan p{};
+  p.nblk = K + (with_root ? 1 : 0);
+  const long rows = static_cast<long>(p.nblk) * V;
+  p.groups = std::max(1L, (rows + static_cast<long>(kTargetCtas) * kWarps * kRows - 1) /
+                              (static_cast<long>(kTargetCtas) * kWarps * kRows));
+  p.rpc = p.groups * kWarps * kRows;
+  p.cph = cdiv(V, p.rpc);
+  p.bgroup = static_cast<int>(std::min<size_t>(16, std::max<size_t>(1, kMaxXBytes / (static_cast<size_t>(H) * esize))));
+  p.bgroup = std::min(p.bgroup, B);
+  const long fc_rows = static_cast<long>(K) * H;
+  p.fc_groups = std::max(1L, (fc_rows + static_cast<long>(kTargetCtas) * kWarps * kRows - 1) /
+                                 (static_cast<long>(kTargetCtas) * kWarps * kRows));
+  p.fc_ctas = static_cast<int>(cdiv(static_cast<int>(fc_rows), p.fc_groups * kWarps * kRows));
+  return p;
+}
+
+struct HeadsWs {
+  void* u;
+  float* cand_v;
+  int* cand_i;
+  int* counters;
+  size_t bytes;
+};
+
+HeadsWs carve_heads_ws(void* base, const HeadsPlan& p, int B, int H, int K, int topk, int esize) {
+  HeadsWs w{};
+  size_t o = 0;
+  auto take = [&](size_t n) { size_t s = o; o = align_up(o + n, 256); return s; };
+  size_t ou = take(static_cast<size_t>(B) * K * H * esize);
+  size_t ncand = static_cast<size_t>(p.nblk) * B * p.cph * topk;
+  size_t ov = take(ncand * 4), oi = take(ncand * 4), oc = take(static_cast<size_t>(p.nblk) * 4);
+  char* c = static_cast<char*>(base);
+  w.u = c ? c + ou : nullptr;
+  w.cand_v = c ? reinterpret_cast<float*>(c + ov) : nullptr;
+  w.cand_i = c ? reinterpret_cast<int*>(c + oi) : nullptr;
+  w.counters = c ? reinterpret_cast<int*>(c + oc) : nullptr;
+  w.bytes = o;
+  return w;
+}
+
+// K1: one warp pass = kRows rows of W1 (flattened [K*H] rows) against nb rows of h.
+template <typename T, int BMAX>
+__global__ void __launch_bounds__(kThreads) heads_fc_kernel(const T* __restrict__ h, const T* __restrict__ W1,
+                                                            const T* __restrict__ b1, int H, int K, int nb,
+                                                            int groups, T* __restrict__ u) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  T* xs = reinterpret_cast<T*>(smem_raw);
+  stage_rows(xs, h, H, nb, H);
+  __syncthreads();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long nrows = static_cast<long>(K) * H;
+  for (int g = 0; g < groups; ++g) {
+    const long row0 = (static_cast<long>(blockIdx.x) * groups * kWarps + static_cast<long>(g) * kWarps + warp) * kRows;
+    if (row0 >= nrows) break;
+    const int valid = nrows - row0 < kRows ? static_cast<int>(nrows - row0) : kRows;
+    float acc[kRows][BMAX];
+    gemv_rows<T, BMAX, kRows, Unroll<BMAX>::U>(W1, row0, valid, H, xs, nb, acc);
+#pragma unroll
+    for (int r = 0; r < kRows; ++r) {
+#pragma unroll
+      for (int b = 0; b < BMAX; ++b) {
+        if (r < valid && b < nb && lane == ((r * BMAX + b) & 31)) {
+          const long row = row0 + r;
+          const int i = static_cast<int>(row % H);
+          const float a = acc[r][b] + Elem<T>::to_f(b1[row]);
+          const float silu = a / (1.0f + expf(-a));  // SiLU(a) = a * sigmoid(a)
+          const float val = Elem<T>::to_f(xs[static_cast<size_t>(b) * H + i]) + silu;
+          u[static_cast<size_t>(b) * nrows + row] = Elem<T>::from_f(val);
+        }
+      }
+    }
+  }
+}
+
+// K2: CTA = slice [v0, v0+rpc) of one block's vocabulary rows.  Block j < K is
+// head j (weights W2_j, activations u[:, j]); block K is lm_head on h (root).
+template <typename T, int BMAX>
+__global__ void __launch_bounds__(kThreads) heads_vocab_kernel(
+    const T* __restrict__ h, const T* __restrict__ u, const T* __restrict__ W2, const T* __restrict__ lm_head,
+    int B, int b0, int nb, int H, int V, int K, int topk, int groups, int rpc, int cph,
+    float* __restrict__ head_logits, int32_t* __restrict__ topk_ids, float* __restrict__ topk_vals,
+    int32_t* __restrict__ root_tok, float* __restrict__ cand_v, int* __restrict__ cand_i, int* __restrict__ counters) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  const int blk = blockIdx.x / cph, cta = blockIdx.x % cph;
+  const bool is_root = blk == K;
+  const int kk = is_root ? 1 : topk;
+  const T* W = is_root ? lm_head : W2 + static_cast<size_t>(blk) * V * H;
+  const T* x = is_root ? h + static_cast<size_t>(b0) * H : u + (static_cast<size_t>(b0) * K + blk) * H;
+  const size_t x_stride = is_root ? H : static_cast<size_t>(K) * H;
+
+  T* xs = reinterpret_cast<T*>(smem_raw);
+  float* zs = reinterpret_cast<float*>(smem_raw + align_up(static_cast<size_t>(nb) * H * sizeof(T), 16));
+  float* mv = zs + static_cast<size_t>(BMAX) * rpc;          // merge buffer values [cph * topk]
+  int* mi = reinterpret_cast<int*>(mv + static_cast<size_t>(cph) * topk);
+  float* sv = reinterpret_cast<float*>(mi + static_cast<size_t>(cph) * topk);  // [kWarps * topk]
+  int* si = reinterpret_cast<int*>(sv + kWarps * topk);
+  float* fv = reinterpret_cast<float*>(si + kWarps * topk);  // [topk] final
+  int* fi = reinterpret_cast<int*>(fv + topk);
+  __shared__ int s_last;
+
+  stage_rows(xs, x, x_stride, nb, H);
+  __syncthreads();
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int v0 = cta * rpc;
+  const int n = min(rpc, V - v0);
+  for (int g = 0; g < groups; ++g) {
+    const int lr0 = (g * kWarps + warp) * kRows;
+    if (lr0 >= n) break;
+    const int valid = min(kRows, n - lr0);
+    float acc[kRows][BMAX];
+    gemv_rows<T, BMAX, kRows, Unroll<BMAX>::U>(W, static_cast<size_t>(v0 + lr0), valid, H, xs, nb, acc);
+#pragma unroll
+    for (int r = 0; r < kRows; ++r) {
+#pragma unroll
+      for (int b = 0; b < BMAX; ++b) {
+        if (r < valid && b < nb && lane == ((r * BMAX + b) & 31)) {
+          zs[static_cast<size_t>(b) * rpc + lr0 + r] = acc[r][b];
+          if (head_logits && !is_root)
+            head_logits[(static_cast<size_t>(b0 + b) * K + blk) * V + v0 + lr0 + r] = acc[r][b];
+        }
+      }
+    }
+  }
+  __syncthreads();
+
+  // local top-k of this slice, per batch row
+  for (int b = 0; b < nb; ++b) {
+    float* outv = cand_v + ((static_cast<size_t>(blk) * B + b0 + b) * cph + cta) * topk;
+    int* outi = cand_i + ((static_cast<size_t>(blk) * B + b0 + b) * cph + cta) * topk;
+    block_topk(zs + static_cast<size_t>(b) * rpc, nullptr, v0, n, kk, mv, mi, sv, si);
+    for (int t = threadIdx.x; t < kk; t += blockDim.x) { outv[t] = mv[t]; outi[t] = mi[t]; }
+    __syncthreads();
+  }
+
+  // the last CTA of this block merges every slice's candidates
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) s_last = (atomicAdd(counters + blk, 1) == cph - 1);
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  for (int b = 0; b < nb; ++b) {
+    const size_t base = (static_cast<size_t>(blk) * B + b0 + b) * cph * topk;
+    const int m = cph * kk;
+    for (int e = threadIdx.x; e < m; e += blockDim.x) {
+      const int c = e / kk, t = e % kk;
+      mv[e] = __ldcg(cand_v + base + static_cast<size_t>(c) * topk + t);
+      mi[e] = __ldcg(cand_i + base + static_cast<size_t>(c) * topk + t);
+    }
+    __syncthreads();
+    block_topk(mv, mi, 0, m, kk, fv, fi, sv, si);
+    if (is_root) {
+      if (threadIdx.x == 0) root_tok[b0 + b] = fi[0];
+    } else {
+      for (int t = threadIdx.x; t < topk; t += blockDim.x) {
+        topk_ids[(static_cast<size_t>(b0 + b) * K + blk) * topk + t] = fi[t];
+        topk_vals[(static_cast<size_t>(b0 + b) * K + blk) * topk + t] = fv[t];
+      }
+    }
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) counters[blk] = 0;  // ready for the next launch
+}
+
+template <typename T, int BMAX>
+int launch_heads(const HeadsPlan& p, const HeadsWs& w, const T* h, const T* W1, const T* b1, const T* W2,
+                 const T* lm, int B, int b0, int nb, int H, int V, int K, int topk, float* head_logits,
+                 int32_t* topk_ids, float* topk_vals, int32_t* root_tok, cudaStream_t st) {
+  const size_t xbytes = align_up(static_cast<size_t>(nb) * H * sizeof(T), 16);
+  auto fc = heads_fc_kernel<T, BMAX>;
+  if (cudaFuncSetAttribute(fc, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(xbytes)) != cudaSuccess)
+    return MEDUSA_ERR_CUDA;
+  fc<<<p.fc_ctas, kThreads, xbytes, st>>>(h + static_cast<size_t>(b0) * H, W1, b1, H, K, nb, p.fc_groups,
+                                          static_cast<T*>(w.u) + static_cast<size_t>(b0) * K * H);
+  MEDUSA_LAUNCH_CHECK();
+  const size_t smem = xbytes + (static_cast<size_t>(BMAX) * p.rpc + 2 * static_cast<size_t>(p.cph) * topk +
+                                2 * kWarps * static_cast<size_t>(topk) + 2 * static_cast<size_t>(topk)) * 4;
+  auto vk = heads_vocab_kernel<T, BMAX>;
+  if (cudaFuncSetAttribute(vk, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) != cudaSuccess)
+    return MEDUSA_ERR_CUDA;
+  vk<<<p.nblk * p.cph, kThreads, smem, st>>>(h, static_cast<const T*>(w.u), W2, lm, B, b0, nb, H, V, K, topk,
+                                             p.groups, p.rpc, p.cph, head_logits, topk_ids, topk_vals, root_tok,
+                                             w.cand_v, w.cand_i, w.counters);
+  MEDUSA_LAUNCH_CHECK();
+  return MEDUSA_OK;
+}
+
+template <typename T>
+int heads_dispatch(const HeadsPlan& p, const HeadsWs& w, const T* h, const T* W1, const T* b1, const T* W2,
+                   const T* lm, int B, int H, int V, int K, int topk, float* hl, int32_t* ids, float* vals,
+                   int32_t* root, cudaStream_t st) {
+  for (int b0 = 0; b0 < B; b0 += p.bgroup) {
+    const int nb = std::min(p.bgroup, B - b0);
+    int rc;
+    if (nb == 1) rc = launch_heads<T, 1>(p, w, h, W1, b1, W2, lm, B, b0, nb, H, V, K, topk, hl, ids, vals, root, st);
+    else if (nb == 2) rc = launch_heads<T, 2>(p, w, h, W1, b1, W2, lm, B, b0, nb, H, V, K, topk, hl, ids, vals, root, st);
+    else if (nb <= 4) rc = launch_heads<T, 4>(p, w, h, W1, b1, W2, lm, B, b0, nb, H, V, K, topk, hl, ids, vals, root, st);
+    else if (nb <= 8) rc = launch_heads<T, 8>(p, w, h, W1, b1, W2, lm, B, b0, nb, H, V, K, topk, hl, ids, vals, root, st);
+    else rc = launch_heads<T, 16>(p, w, h, W1, b1, W2, lm, B, b0, nb, H, V, K, topk, hl, ids, vals, root, st);
+    if (rc != MEDUSA_OK) return rc;
+  }
+  return MEDUSA_OK;
+}
+
+}  // namespace
+
+MEDUSA_API size_t medusa_heads_topk_workspace_size(int32_t B, int32_t H, int32_t V, int32_t K, int32_t topk,
+                                                   int32_t with_lm_head, medusa_dtype dtype) {
+  if (B < 1 || H < 8 || V < 1 || K < 1 || topk < 1) return 0;
+  const int es = dtype == MEDUSA_BF16 ? 2 : 4;
+  HeadsPlan p = plan_heads(B, H, V, K, with_lm_head, es);
+  return carve_heads_ws(nullptr, p, B, H, K, topk, es).bytes;
+}
+
+MEDUSA_API int medusa_heads_topk(const void* h, const void* w1, const void* b1, const void* w2, const void* lm_head,
+                                 int32_t B, int32_t H, int32_t V, int32_t K, int32_t topk, medusa_dtype dtype,
+                                 float* head_logits, int32_t* topk_ids, float* topk_vals, int32_t* root_tok,
+                                 void* ws, size_t ws_bytes, medusa_stream_t stream) {
+  if (!h || !w1 || !b1 || !w2 || !topk_ids || !topk_vals || !root_tok) return MEDUSA_ERR_INVALID_ARG;
+  if (dtype != MEDUSA_F32 && dtype != MEDUSA_BF16) return MEDUSA_ERR_INVALID_ARG;
+  if (B < 1 || B > MEDUSA_MAX_BATCH || K < 1 || V < 1 || H < 8 || topk < 1 || topk > MEDUSA_MAX_TOPK || topk > V)
+    return MEDUSA_ERR_INVALID_ARG;
+  if (H % 8 != 0) return MEDUSA_ERR_UNSUPPORTED;
+  const void* ptrs[] = {h, w1, b1, w2, topk_ids, topk_vals, root_tok, ws};
+  for (const void* q : ptrs)
+    if (q && !aligned16(q)) return MEDUSA_ERR_ALIGNMENT;
+  if ((lm_head && !aligned16(lm_head)) || (head_logits && !aligned16(head_logits))) return MEDUSA_ERR_ALIGNMENT;
+  const int es = dtype == MEDUSA_BF16 ? 2 : 4;
+  HeadsPlan p = plan_heads(B, H, V, K, lm_head != nullptr, es);
+  HeadsWs w = carve_heads_ws(ws, p, B, H, K, topk, es);
+  if (!ws || ws_bytes < w.bytes) return MEDUSA_ERR_WORKSPACE;
+  auto st = reinterpret_cast<cudaStream_t>(stream);
+  if (dtype == MEDUSA_BF16)
+    return heads_dispatch(p, w, static_cast<const __nv_bfloat16*>(h), static_cast<const __nv_bfloat16*>(w1),
+                          static_cast<const __nv_bfloat16*>(b1), static_cast<const __nv_bfloat16*>(w2),
+                          static_cast<const __nv_bfloat16*>(lm_head), B, H, V, K, topk, head_logits, topk_ids,
+                          topk_vals, root_tok, st);
+  return heads_dispatch(p, w, static_cast<const float*>(h), static_cast<const float*>(w1),
+                        static_cast<const float*>(b1), static_cast<const float*>(w2),
+                        static_cast<const float*>(lm_head), B, H, V, K, topk, head_logits, topk_ids, topk_vals,
+                        root_tok, st);
+}

@@ -1,0 +1,564 @@
+// Verification (K5) and typical acceptance (K6).
+//
+// wiblog.cn "Medusa multi-head speculative decoding", section "Inference flow
+// in an online chat service": the original model computes, in one pass, the
+// probability of every candidate token in the tree; section "Typical
+// acceptance": a candidate is kept when its probability exceeds the minimum of
+// a hard threshold and an entropy-dependent threshold, the first token is
+// always taken greedily, the longest passing prefix is output, and at
+// temperature zero the scheme is greedy decoding.  cnnetsun.cn "Medusa safety
+// considerations", section "Posterior probability evaluation":
+// evaluate_posterior(logits, candidates, temperature, posterior_threshold,
+// posterior_alpha) -> best_candidate, accept_length.
+//
+// K5 (bf16): logits = X lm_head^T for every tree node is a GEMM with M = tree
+// rows (B*T) and N = vocabulary.  tcgen05.mma accumulates a 128 x BN tile in
+// TMEM from TMA-fed, 128-byte-swizzled shared-memory stages (one producer
+// thread, one MMA thread).  The epilogue (4 warps, one TMEM lane = one tree
+// node each) never writes the logits unless asked: it reduces its vocabulary
+// tile to (max, argmax, sum of exp, sum of exp * logit) at the temperature and
+// picks out the logits of the node's children tokens.
+// K5 (fp32): CUDA-core GEMV into a logits buffer, then the same statistics.
+// K6a merges the per-tile statistics of every node; K6b decides acceptance,
+// the longest kept prefix, the next root, one CTA per request.
+#include <algorithm>
+#include <mutex>
+
+#include "gemv.cuh"
+#include "tc.cuh"
+#include "tree.cuh"
+
+using namespace medusa;
+
+namespace medusa {
+
+EncodeTiledFn encode_tiled_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+bool make_tmap_bf16(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+  EncodeTiledFn enc = encode_tiled_fn();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {64, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace medusa
+
+namespace {
+
+constexpr int BM = 128;
+constexpr int BK = 64;
+constexpr int STAGES = 4;
+constexpr int F32_TILE = 256;  // vocabulary columns per statistics tile on the fp32 path
+
+struct VerifyPlan {
+  int R, BN, n_mt, n_nt;
+};
+
+VerifyPlan plan_verify(int B, int T, int V, medusa_dtype dt) {
+  VerifyPlan p{};
+  p.R = B * T;
+  if (dt == MEDUSA_BF16) {
+    p.n_mt = cdiv(p.R, BM);
+    if (p.n_mt == 1)
+      p.BN = std::min(256, std::max(16, cdiv(cdiv(V, 148), 16) * 16));
+    else
+      p.BN = 256;
+    p.n_nt = cdiv(V, p.BN);
+  } else {
+    p.n_mt = 1;
+    p.BN = F32_TILE;
+    p.n_nt = cdiv(V, F32_TILE);
+  }
+  return p;
+}
+
+struct VerifyWs {
+  float4* part;      // [R, n_nt] (max, sum exp, sum exp*y, argmax bits)
+  float* child_z;    // [R] logit of node c's token under its parent (indexed by c)
+  float4* rowst;     // [R] merged statistics
+  float* zbuf;       // fp32 path: [R, V] logits when the caller gives none
+  size_t bytes;
+};
+
+VerifyWs carve_verify_ws(void* base, const VerifyPlan& p, int V, medusa_dtype dt) {
+  VerifyWs w{};
+  size_t o = 0;
+  auto take = [&](size_t n) { size_t s = o; o = align_up(o + n, 256); return s; };
+  size_t op = take(static_cast<size_t>(p.R) * p.n_nt * 16), oc = take(static_cast<size_t>(p.R) * 4),
+         orow = take(static_cast<size_t>(p.R) * 16);
+  size_t oz = dt == MEDUSA_F32 ? take(static_cast<size_t>(p.R) * V * 4) : 0;
+  char* c = static_cast<char*>(base);
+  if (c) {
+    w.part = reinterpret_cast<float4*>(c + op);
+    w.child_z = reinterpret_cast<float*>(c + oc);
+    w.rowst = reinterpret_cast<float4*>(c + orow);
+    w.zbuf = dt == MEDUSA_F32 ? reinterpret_cast<float*>(c + oz) : nullptr;
+  }
+  w.bytes = o;
+  return w;
+}
+
+struct EpiArgs {
+  int R, V, T, n_nt;
+  const int32_t* tokens;
+  medusa_tree_dev tr;
+  float inv_tau;  // 0 at temperature 0 (statistics beyond max/argmax skipped)
+  float* logits;
+  float4* part;
+  float* child_z;
+  int32_t* dev_status;
+};
+
+// ------------------------------------------------------------------------
+// K5, bf16: tcgen05 GEMM with the statistics epilogue.
+// 192 threads: warps 0-3 epilogue (TMEM lanes 0-127), warp 4 TMA producer,
+// warp 5 MMA issuer and TMEM owner.
+// ------------------------------------------------------------------------
+template <int BN>
+__global__ void __launch_bounds__(192, 1) verify_tc_kernel(const __grid_constant__ CUtensorMap tma_x,
+                                                          const __grid_constant__ CUtensorMap tma_w, int H,
+                                                          int n_mt, EpiArgs ea) {
+  extern __shared__ __align__(1024) unsigned char tc_smem_raw[];
+  constexpr uint32_t A_BYTES = BM * BK * 2;
+  constexpr uint32_t B_BYTES = BN * BK * 2;
+  constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
+  constexpr uint32_t TMEM_COLS = BN <= 32 ? 32 : BN <= 64 ? 64 : BN <= 128 ? 128 : 256;
+  unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(tc_smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  uint64_t* empty = full + STAGES;
+  uint64_t* accb = empty + STAGES;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accb + 1);
+  __shared__ int s_fail;
+
+  const int tile = blockIdx.x;
+  const int m_t = tile % n_mt, n_t = tile / n_mt;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nk = cdiv(H, BK);
+
+  if (threadIdx.x == 0) {
+    s_fail = 0;
+    for (int s = 0; s < STAGES; ++s) {
+      tc::mbar_init(full + s, 1);
+      tc::mbar_init(empty + s, 1);
+    }
+    tc::mbar_init(accb, 1);
+    tc::fence_mbar_init();
+    tc::prefetch_tmap(&tma_x);
+    tc::prefetch_tmap(&tma_w);
+  }
+  if (warp == 5) tc::tmem_alloc(tmem_slot, TMEM_COLS);
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t taddr = *tmem_slot;
+
+  if (warp == 4) {
+    if (lane == 0) {
+      for (int kb = 0; kb < nk; ++kb) {
+        const int s = kb % STAGES;
+        const uint32_t ph = (kb / STAGES) & 1;
+        if (!tc::mbar_wait(empty + s, ph ^ 1)) { s_fail = 1; break; }
+        const uint32_t sa = smem_u32(smem + s * STAGE_BYTES);
+        tc::mbar_expect_tx(full + s, STAGE_BYTES);
+        tc::tma_load_2d(sa, &tma_x, kb * BK, m_t * BM, full + s);
+        tc::tma_load_2d(sa + A_BYTES, &tma_w, kb * BK, n_t * BN, full + s);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 5) {
+    if (lane == 0) {
+      constexpr uint32_t idesc = tc::idesc_bf16_f32(BM, BN);
+      for (int kb = 0; kb < nk; ++kb) {
+        const int s = kb % STAGES;
+        const uint32_t ph = (kb / STAGES) & 1;
+        if (!tc::mbar_wait(full + s, ph)) { s_fail = 1; break; }
+        tc::fence_after_sync();
+        const uint32_t sa = smem_u32(smem + s * STAGE_BYTES);
+#pragma unroll
+        for (int k = 0; k < BK / 16; ++k) {
+          const uint64_t ad = tc::smem_desc_sw128(sa + k * 32);
+          const uint64_t bd = tc::smem_desc_sw128(sa + A_BYTES + k * 32);
+          tc::mma_bf16(taddr, ad, bd, idesc, (kb | k) != 0);
+        }
+        tc::mma_commit(empty + s);
+      }
+      tc::mma_commit(accb);  // fires once every issued MMA has completed
+    }
+    __syncwarp();
+  } else {
+    // ---- epilogue: thread = one tree-node row of this tile ----
+    const bool ok = tc::mbar_wait(accb, 0);
+    tc::fence_after_sync();
+    const int row = warp * 32 + lane;
+    const int r = m_t * BM + row;
+    const bool valid_row = r < ea.R;
+    const uint32_t tl = taddr + (static_cast<uint32_t>(warp * 32) << 16);
+    const int n0 = n_t * BN;
+    float m = -INFINITY;
+    int arg = n0;
+    bool nan_seen = false;
+    int b = 0, node = 0, c_beg = 0, c_cnt = 0;
+    if (valid_row) {
+      b = r / ea.T;
+      node = r % ea.T;
+      c_beg = ea.tr.child_start[node];
+      c_cnt = ea.tr.child_count[node];
+    }
+#pragma unroll 1
+    for (int c0 = 0; c0 < BN; c0 += 32) {
+      float v[32];
+      tc::tmem_ld32(tl + c0, v);
+      if (!valid_row || !ok) continue;
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const int col = n0 + c0 + j;
+        if (c0 + j < BN && col < ea.V) {
+          if (v[j] > m) { m = v[j]; arg = col; }
+          nan_seen |= v[j] != v[j];
+        }
+      }
+      if (ea.logits) {
+        float* dst = ea.logits + static_cast<size_t>(r) * ea.V + n0 + c0;
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if (c0 + j < BN && n0 + c0 + j < ea.V) dst[j] = v[j];
+      }
+      for (int c = c_beg; c < c_beg + c_cnt; ++c) {
+        const int rel = ea.tokens[static_cast<size_t>(b) * ea.T + c] - (n0 + c0);
+        if (rel >= 0 && rel < 32 && c0 + rel < BN) {
+          float z = 0.f;
+#pragma unroll
+          for (int j = 0; j < 32; ++j) z = (j == rel) ? v[j] : z;
+          ea.child_z[static_cast<size_t>(b) * ea.T + c] = z;
+        }
+      }
+    }
+    float s = 0.f, w = 0.f;
+    if (ea.inv_tau > 0.f) {
+#pragma unroll 1
+      for (int c0 = 0; c0 < BN; c0 += 32) {
+        float v[32];
+        tc::tmem_ld32(tl + c0, v);
+        if (!valid_row || !ok) continue;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          if (c0 + j < BN && n0 + c0 + j < ea.V) {
+            const float y = (v[j] - m) * ea.inv_tau;
+            const float e = expf(y);
+            s += e;
+            w = fmaf(e, y, w);
+          }
+        }
+      }
+    }
+    if (valid_row) {
+      if (nan_seen) s = __int_as_float(0x7fc00000);
+      ea.part[static_cast<size_t>(r) * ea.n_nt + n_t] = make_float4(m, s, w, __int_as_float(arg));
+      if ((!ok || s_fail) && ea.dev_status) atomicOr(ea.dev_status + b, MEDUSA_DEV_TIMEOUT);
+    }
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 5) tc::tmem_dealloc(taddr, TMEM_COLS);
+}
+
+// ------------------------------------------------------------------------
+// K5, fp32: GEMV logits, then per-(row, tile) statistics.
+// ------------------------------------------------------------------------
+constexpr int kThreads = 256, kWarps = 8, kRows = 4;
+
+template <int BMAX>
+__global__ void __launch_bounds__(kThreads) verify_gemv_f32_kernel(const float* __restrict__ x,
+                                                                   const float* __restrict__ lm, int r0, int nb,
+                                                                   int H, int V, int groups, float* __restrict__ z) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  float* xs = reinterpret_cast<float*>(smem_raw);
+  stage_rows(xs, x + static_cast<size_t>(r0) * H, H, nb, H);
+  __syncthreads();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int g = 0; g < groups; ++g) {
+    const long v0 = (static_cast<long>(blockIdx.x) * groups * kWarps + static_cast<long>(g) * kWarps + warp) * kRows;
+    if (v0 >= V) break;
+    const int valid = V - v0 < kRows ? static_cast<int>(V - v0) : kRows;
+    float acc[kRows][BMAX];
+    gemv_rows<float, BMAX, kRows, 2>(lm, static_cast<size_t>(v0), valid, H, xs, nb, acc);
+#pragma unroll
+    for (int rr = 0; rr < kRows; ++rr)
+#pragma unroll
+      for (int bb = 0; bb < BMAX; ++bb)
+        if (rr < valid && bb < nb && lane == ((rr * BMAX + bb) & 31))
+          z[static_cast<size_t>(r0 + bb) * V + v0 + rr] = acc[rr][bb];
+  }
+}
+
+__global__ void __launch_bounds__(256) verify_stats_kernel(const float* __restrict__ z, EpiArgs ea) {
+  const int t = blockIdx.x, r = blockIdx.y;
+  const int n0 = t * F32_TILE;
+  const int col = n0 + threadIdx.x;
+  const float v = col < ea.V ? z[static_cast<size_t>(r) * ea.V + col] : -INFINITY;
+  __shared__ float sm[8];
+  __shared__ int si[8];
+  __shared__ float sw[8];
+  float m = col < ea.V ? v : -INFINITY;
+  int arg = col < ea.V ? col : 0x7fffffff;
+  if (m != m) { m = -INFINITY; }
+  warp_argmax(m, arg);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (lane == 0) { sm[warp] = m; si[warp] = arg; }
+  __syncthreads();
+  m = -INFINITY;
+  arg = 0x7fffffff;
+  for (int i = 0; i < 8; ++i)
+    if (better(sm[i], si[i], m, arg)) { m = sm[i]; arg = si[i]; }
+  if (arg == 0x7fffffff) arg = n0;
+  float s = 0.f, w = 0.f;
+  if (col < ea.V && ea.inv_tau > 0.f) {
+    const float y = (v - m) * ea.inv_tau;
+    s = expf(y);
+    w = s * y;
+  }
+  s = warp_sum(s);
+  w = warp_sum(w);
+  __syncthreads();
+  if (lane == 0) { sm[warp] = s; sw[warp] = w; }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float S = 0.f, W = 0.f;
+    for (int i = 0; i < 8; ++i) { S += sm[i]; W += sw[i]; }
+    ea.part[static_cast<size_t>(r) * ea.n_nt + t] = make_float4(m, S, W, __int_as_float(arg));
+  }
+  // children whose token lies in this tile
+  const int b = r / ea.T, node = r % ea.T;
+  const int c_beg = ea.tr.child_start[node], c_cnt = ea.tr.child_count[node];
+  for (int c = c_beg + threadIdx.x; c < c_beg + c_cnt; c += blockDim.x) {
+    const int tok = ea.tokens[static_cast<size_t>(b) * ea.T + c];
+    if (tok >= n0 && tok < n0 + F32_TILE && tok < ea.V) ea.child_z[static_cast<size_t>(b) * ea.T + c] = z[static_cast<size_t>(r) * ea.V + tok];
+  }
+}
+
+// ------------------------------------------------------------------------
+// K6a: merge the per-tile statistics of each node (warp per row, fixed order).
+// M = max m_t; S = sum s_t e^{(m_t-M)/tau}; W = sum e^{(m_t-M)/tau} (w_t + s_t (m_t-M)/tau)
+// so that with q = softmax(z/tau): H = ln S - W / S.
+// ------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) verify_merge_kernel(const float4* __restrict__ part, int R, int n_nt,
+                                                           float inv_tau, float4* __restrict__ rowst) {
+  const int r = blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (r >= R) return;
+  const float4* pr = part + static_cast<size_t>(r) * n_nt;
+  float m = -INFINITY;
+  int arg = 0x7fffffff;
+  for (int t = lane; t < n_nt; t += 32) {
+    const float4 q = pr[t];
+    if (better(q.x, __float_as_int(q.w), m, arg)) { m = q.x; arg = __float_as_int(q.w); }
+  }
+  warp_argmax(m, arg);
+  float S = 0.f, W = 0.f;
+  bool nan_seen = false;
+  if (inv_tau > 0.f) {
+    for (int t = lane; t < n_nt; t += 32) {
+      const float4 q = pr[t];
+      nan_seen |= q.y != q.y;
+      if (q.y > 0.f) {
+        const float d = (q.x - m) * inv_tau;
+        const float sc = expf(d);
+        S = fmaf(q.y, sc, S);
+        W = fmaf(sc, fmaf(q.y, d, q.z), W);
+      }
+    }
+    S = warp_sum(S);
+    W = warp_sum(W);
+  } else {
+    for (int t = lane; t < n_nt; t += 32) nan_seen |= pr[t].y != pr[t].y;
+  }
+  nan_seen = __any_sync(0xffffffffu, nan_seen);
+  if (lane == 0) rowst[r] = make_float4(m, nan_seen ? __int_as_float(0x7fc00000) : S, W, __int_as_float(arg));
+}
+
+// ------------------------------------------------------------------------
+// K6b: typical acceptance, longest kept prefix, next root.  CTA = request.
+// ------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) accept_kernel(medusa_tree_dev tr, const int32_t* __restrict__ tokens,
+                                                     const float4* __restrict__ rowst,
+                                                     const float* __restrict__ child_z, float inv_tau, float thr,
+                                                     float alpha, float* __restrict__ node_p,
+                                                     float* __restrict__ node_H, int32_t* __restrict__ accept_len,
+                                                     int32_t* __restrict__ best_path, int32_t* __restrict__ best_node,
+                                                     int32_t* __restrict__ accepted_tokens,
+                                                     int32_t* __restrict__ next_root, int32_t* __restrict__ dev_status) {
+  extern __shared__ unsigned char s_acc[];  // [T] own test passed, then kept
+  __shared__ int s_best, s_path, s_nan;
+  const int b = blockIdx.x;
+  const int T = tr.T;
+  const size_t base = static_cast<size_t>(b) * T;
+  if (threadIdx.x == 0) { s_best = 0; s_path = 0x7fffffff; s_nan = 0; }
+  for (int c = threadIdx.x; c < T; c += blockDim.x) {
+    const float4 own = rowst[base + c];
+    if (node_H) {
+      float H = 0.f;
+      if (inv_tau > 0.f) H = logf(own.y) - own.z / own.y;
+      node_H[base + c] = H;
+    }
+    if (own.x != own.x || own.y != own.y) s_nan = 1;
+    if (c == 0) {
+      s_acc[0] = 1;
+      if (node_p) node_p[base] = 1.f;
+      continue;
+    }
+    const float4 par = rowst[base + tr.parent[c]];
+    const int32_t tok = tokens[base + c];
+    bool a;
+    float p;
+    if (inv_tau > 0.f) {
+      const float H = logf(par.y) - par.z / par.y;
+      p = expf((child_z[base + c] - par.x) * inv_tau) / par.y;
+      a = p > fminf(thr, alpha * expf(-H));
+    } else {
+      a = tok == __float_as_int(par.w);
+      p = a ? 1.f : 0.f;
+    }
+    s_acc[c] = a ? 1 : 0;
+    if (node_p) node_p[base + c] = p;
+  }
+  __syncthreads();
+  for (int d = 1; d <= tr.dmax; ++d) {
+    for (int c = threadIdx.x; c < T; c += blockDim.x)
+      if (tr.depth[c] == d) s_acc[c] = s_acc[c] && s_acc[tr.parent[c]];
+    __syncthreads();
+  }
+  // deepest kept node, ties to the lowest canonical index
+  int key = 0xFFFF;  // root: depth 0, index 0
+  for (int c = threadIdx.x; c < T; c += blockDim.x)
+    if (s_acc[c]) key = max(key, (tr.depth[c] << 16) | (0xFFFF - c));
+  for (int o = 16; o > 0; o >>= 1) key = max(key, __shfl_xor_sync(0xffffffffu, key, o));
+  if ((threadIdx.x & 31) == 0) atomicMax(&s_best, key);
+  __syncthreads();
+  const int best = 0xFFFF - (s_best & 0xFFFF);
+  for (int p = threadIdx.x; p < tr.P; p += blockDim.x) {
+    const int leaf = tr.leaf[p];
+    if ((tr.mask[static_cast<size_t>(leaf) * tr.mask_words + best / 32] >> (best % 32)) & 1u) atomicMin(&s_path, p);
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const int a = tr.depth[best];
+    accept_len[b] = a;
+    best_node[b] = best;
+    best_path[b] = s_path;
+    next_root[b] = __float_as_int(rowst[base + best].w);
+    int32_t* out = accepted_tokens + static_cast<size_t>(b) * (tr.dmax + 1);
+    for (int d = a + 1; d <= tr.dmax; ++d) out[d] = -1;
+    for (int n = best; n >= 0; n = tr.parent[n]) out[tr.depth[n]] = tokens[base + n];
+    if (s_nan && dev_status) atomicOr(dev_status + b, MEDUSA_DEV_NAN);
+  }
+}
+
+template <int BN>
+int launch_tc(const VerifyPlan& p, const CUtensorMap& mx, const CUtensorMap& mw, int H, const EpiArgs& ea,
+              cudaStream_t st) {
+  const size_t smem = 1024 + STAGES * (static_cast<size_t>(BM) * BK * 2 + static_cast<size_t>(BN) * BK * 2) + 256;
+  auto k = verify_tc_kernel<BN>;
+  if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) != cudaSuccess)
+    return MEDUSA_ERR_CUDA;
+  k<<<p.n_mt * p.n_nt, 192, smem, st>>>(mx, mw, H, p.n_mt, ea);
+  MEDUSA_LAUNCH_CHECK();
+  return MEDUSA_OK;
+}
+
+int dispatch_tc(const VerifyPlan& p, const CUtensorMap& mx, const CUtensorMap& mw, int H, const EpiArgs& ea,
+                cudaStream_t st) {
+  switch (p.BN) {
+#define MEDUSA_BN(n) case n: return launch_tc<n>(p, mx, mw, H, ea, st);
+    MEDUSA_BN(16) MEDUSA_BN(32) MEDUSA_BN(48) MEDUSA_BN(64) MEDUSA_BN(80) MEDUSA_BN(96) MEDUSA_BN(112)
+    MEDUSA_BN(128) MEDUSA_BN(144) MEDUSA_BN(160) MEDUSA_BN(176) MEDUSA_BN(192) MEDUSA_BN(208) MEDUSA_BN(224)
+    MEDUSA_BN(240) MEDUSA_BN(256)
+#undef MEDUSA_BN
+    default: return MEDUSA_ERR_UNSUPPORTED;
+  }
+}
+
+}  // namespace
+
+MEDUSA_API size_t medusa_verify_accept_workspace_size(const medusa_tree* tree, int32_t B, int32_t H, int32_t V,
+                                                      medusa_dtype dtype) {
+  if (!tree || B < 1 || H < 1 || V < 1) return 0;
+  VerifyPlan p = plan_verify(B, tree->T, V, dtype);
+  return carve_verify_ws(nullptr, p, V, dtype).bytes;
+}
+
+MEDUSA_API int medusa_verify_accept(const medusa_tree* tree, const void* x, const void* lm_head,
+                                    const int32_t* tree_tokens, int32_t B, int32_t H, int32_t V, medusa_dtype dtype,
+                                    float temperature, float posterior_threshold, float posterior_alpha,
+                                    float* logits, float* node_p, float* node_H, int32_t* accept_len,
+                                    int32_t* best_path, int32_t* best_node, int32_t* accepted_tokens,
+                                    int32_t* next_root, int32_t* dev_status, void* ws, size_t ws_bytes,
+                                    medusa_stream_t stream) {
+  if (!tree || !x || !lm_head || !tree_tokens || !accept_len || !best_path || !best_node || !accepted_tokens ||
+      !next_root)
+    return MEDUSA_ERR_INVALID_ARG;
+  if (B < 1 || B > MEDUSA_MAX_BATCH || H < 8 || V < 1 || !(temperature >= 0.f)) return MEDUSA_ERR_INVALID_ARG;
+  if (dtype != MEDUSA_F32 && dtype != MEDUSA_BF16) return MEDUSA_ERR_INVALID_ARG;
+  if (H % 8 != 0) return MEDUSA_ERR_UNSUPPORTED;
+  const void* ptrs[] = {x, lm_head, tree_tokens, accept_len, best_path, best_node, accepted_tokens, next_root};
+  for (const void* q : ptrs)
+    if (!aligned16(q)) return MEDUSA_ERR_ALIGNMENT;
+  const void* opt[] = {logits, node_p, node_H, dev_status, ws};
+  for (const void* q : opt)
+    if (q && !aligned16(q)) return MEDUSA_ERR_ALIGNMENT;
+  const int T = tree->T;
+  VerifyPlan p = plan_verify(B, T, V, dtype);
+  VerifyWs w = carve_verify_ws(ws, p, V, dtype);
+  if (!ws || ws_bytes < w.bytes) return MEDUSA_ERR_WORKSPACE;
+  auto st = reinterpret_cast<cudaStream_t>(stream);
+  const float inv_tau = temperature > 0.f ? 1.f / temperature : 0.f;
+  EpiArgs ea{p.R, V, T, p.n_nt, tree_tokens, tree->dev, inv_tau, logits, w.part, w.child_z, dev_status};
+
+  if (dtype == MEDUSA_BF16) {
+    CUtensorMap mx, mw;
+    if (!make_tmap_bf16(&mx, x, p.R, H, BM) || !make_tmap_bf16(&mw, lm_head, V, H, p.BN)) return MEDUSA_ERR_CUDA;
+    const int rc = dispatch_tc(p, mx, mw, H, ea, st);
+    if (rc != MEDUSA_OK) return rc;
+  } else {
+    float* z = logits ? logits : w.zbuf;
+    ea.logits = nullptr;
+    const int rows_per_launch = 16;
+    const long vrows = V;
+    const int groups = std::max(1L, (vrows + 148L * 4 * kWarps * kRows - 1) / (148L * 4 * kWarps * kRows));
+    const int ctas = cdiv(V, groups * kWarps * kRows);
+    for (int r0 = 0; r0 < p.R; r0 += rows_per_launch) {
+      const int nb = std::min(rows_per_launch, p.R - r0);
+      const size_t smem = static_cast<size_t>(nb) * H * 4;
+      if (smem > 200 * 1024) return MEDUSA_ERR_UNSUPPORTED;
+      auto k = nb <= 4 ? verify_gemv_f32_kernel<4> : nb <= 8 ? verify_gemv_f32_kernel<8> : verify_gemv_f32_kernel<16>;
+      if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) != cudaSuccess)
+        return MEDUSA_ERR_CUDA;
+      k<<<ctas, kThreads, smem, st>>>(static_cast<const float*>(x), static_cast<const float*>(lm_head), r0, nb, H,
+                                      V, groups, z);
+      MEDUSA_LAUNCH_CHECK();
+    }
+    verify_stats_kernel<<<dim3(p.n_nt, p.R), 256, 0, st>>>(z, ea);
+    MEDUSA_LAUNCH_CHECK();
+  }
+  verify_merge_kernel<<<cdiv(p.R, 8), 256, 0, st>>>(w.part, p.R, p.n_nt, inv_tau, w.rowst);
+  MEDUSA_LAUNCH_CHECK();
+  accept_kernel<<<B, 256, T, st>>>(tree->dev, tree_tokens, w.rowst, w.child_z, inv_tau, posterior_threshold,
+                                   posterior_alpha, node_p, node_H, accept_len, best_path, best_node, accepted_tokens,
+                                   next_root, dev_status);
+  MEDUSA_LAUNCH_CHECK();
+  return MEDUSA_OK;
+}

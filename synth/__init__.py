@@ -202,7 +202,7 @@ class Workload:
     def k_needed(self) -> int:
         if self.topk:
             return self.topk
-        return 1 + max(r for c in self.choices() for r in c)
+        return 1 + max((r for c in self.choices() for r in c), default=0)
 
     def kv_lens(self) -> List[int]:
         if not self.ragged:

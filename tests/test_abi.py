@@ -1,0 +1,100 @@
+"""The C ABI library: it loads without a GPU, exports every entry point the
+header declares, and rejects bad arguments on the host before any launch."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from conftest import ROOT
+
+HEADER = os.path.join(ROOT, "include", "medusa.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from medusa_head_speculative_04_b300 import build
+    build.build()
+    import medusa_head_speculative_04_b300 as m
+    return m
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(medusa_\w+)\s*\(", src)))
+
+
+def test_header_declares_the_five_step_calls():
+    names = declared_functions()
+    for n in ("medusa_heads_topk", "medusa_build_tree", "medusa_tree_attention", "medusa_verify_accept",
+              "medusa_kv_commit"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    missing = [n for n in declared_functions() if not hasattr(lib.lib, n)]
+    assert not missing, missing
+
+
+def test_status_strings(lib):
+    f = lib.lib.medusa_status_string
+    assert f(0) == b"ok"
+    assert b"align" in f(-2)
+    assert f(-99) == b"unknown status"
+
+
+def _tree_create(lib, choices):
+    flat = [r for c in choices for r in c]
+    fa = (ctypes.c_int32 * max(1, len(flat)))(*flat)
+    la = (ctypes.c_int32 * max(1, len(choices)))(*[len(c) for c in choices])
+    h = ctypes.c_void_p()
+    return lib.lib.medusa_tree_create(fa, la, len(choices), ctypes.byref(h))
+
+
+@pytest.mark.parametrize("bad", [[(0,), (1, 0, 0)], [(0,), (0,)], [(0, -1)], [tuple([0] * 17)]])
+def test_tree_create_rejects_bad_specs_on_host(lib, bad):
+    # not prefix-closed, duplicate, negative rank, deeper than MEDUSA_MAX_DEPTH
+    assert _tree_create(lib, bad) == -1
+
+
+def test_tree_create_rejects_too_many_nodes(lib):
+    choices = [(i,) for i in range(64)] + [(i, j) for i in range(64) for j in range(64)]
+    assert _tree_create(lib, choices) == -1
+
+
+def test_heads_host_validation(lib):
+    L = lib.lib
+    p = 0x10000  # aligned fake addresses: never dereferenced, the call fails before any launch
+    # no workspace: every call below must fail on the host, before any launch
+    args = [p] * 5 + [1, 64, 100, 2, 4, 1, None, p, p, p, None, 0, None]
+    assert L.medusa_heads_topk(*args) == -4
+    bad = list(args)
+    bad[0] = None
+    assert L.medusa_heads_topk(*bad) == -1
+    bad = list(args)
+    bad[1] = p + 4
+    assert L.medusa_heads_topk(*bad) == -2
+    bad = list(args)
+    bad[6] = 60          # H not a multiple of 8
+    assert L.medusa_heads_topk(*bad) == -3
+    bad = list(args)
+    bad[9] = 101         # topk > V
+    assert L.medusa_heads_topk(*bad) == -1
+
+
+def test_heads_workspace_size_grows_with_batch(lib):
+    f = lib.lib.medusa_heads_topk_workspace_size
+    a = f(1, 4096, 32000, 5, 10, 0, 1)
+    b = f(16, 4096, 32000, 5, 10, 0, 1)
+    assert 0 < a < b
+    assert f(0, 4096, 32000, 5, 10, 0, 1) == 0
+
+
+def test_binding_has_no_cpu_path():
+    src = open(os.path.join(ROOT, "medusa_head_speculative_04_b300", "_binding.py")).read()
+    assert "import oracle" not in src and "from oracle" not in src
+    for f in os.listdir(os.path.join(ROOT, "medusa_head_speculative_04_b300")):
+        if f.endswith(".py"):
+            s = open(os.path.join(ROOT, "medusa_head_speculative_04_b300", f)).read()
+            assert "oracle" not in s.replace("oracle-free", ""), f

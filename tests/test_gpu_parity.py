@@ -1,0 +1,206 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle,
+element by element, on the same seeded inputs (small and 7B-shaped workloads).
+
+Stage by stage: each stage's oracle runs on the GPU's (already checked)
+discrete outputs of the stage before, so a near-tie upstream (counted, not
+failed) never masks a real mismatch downstream.
+"""
+import dataclasses
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from _util import DELTA, TOL, accept_parity, check_topk, np64, npi, rel_err, step_oracle_inputs
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def mb():
+    assert torch.cuda.is_available(), "the CUDA parity tests need a GPU"
+    import medusa_head_speculative_04_b300 as m
+    return m
+
+
+def make_step(mb, wl, inp, root_from_lm=False, **kw):
+    return mb.MedusaStep(inp.choices, wl.B, wl.H, wl.V, wl.K, wl.Hq, wl.Hkv, wl.D, wl.Lmax, wl.k_needed(),
+                         inp.dtype, root_from_lm_head=root_from_lm, keep_head_logits=True, keep_logits=True,
+                         **kw)
+
+
+def run_step(mb, wl, inp, temperature, root_from_lm=False, **kw):
+    step = make_step(mb, wl, inp, root_from_lm, **kw)
+    kc, vc, kl = inp.k_cache.clone(), inp.v_cache.clone(), inp.kv_len.clone()
+    step.run(inp.h, inp.W1, inp.b1, inp.W2, inp.lm_head, inp.X, inp.q, inp.k_new, inp.v_new, kc, vc, kl,
+             temperature, wl.posterior_threshold, wl.posterior_alpha, root=inp.root)
+    torch.cuda.synchronize()
+    return step, kc, vc, kl
+
+
+def check_full(wl, inp, step, kc, vc, kl, temperature, root_from_lm=False):
+    """Whole-step parity with the oracle computing every output."""
+    kind = wl.dtype
+    tol, delta = TOL[kind], DELTA[kind]
+    o = step_oracle_inputs(inp)
+    near = 0
+    # heads + top-k
+    _, z_o = oracle.medusa_heads(o["h"], o["W1"], o["b1"], o["W2"], u_bf16=(kind == "bf16"))
+    assert rel_err(step.head_logits, z_o) < tol
+    k = wl.k_needed()
+    near += check_topk(step.topk_ids, step.topk_vals, z_o, k, delta)
+    ids = npi(step.topk_ids)
+    vals_o = np.take_along_axis(z_o, ids, axis=-1)
+    assert rel_err(step.topk_vals, vals_o) < tol
+    if root_from_lm:
+        z_root = o["h"] @ o["lm_head"].T
+        for b in range(wl.B):
+            g, r = int(step.root[b]), int(oracle.base_root(o["h"][b:b + 1], o["lm_head"])[0])
+            if g != r:
+                assert abs(z_root[b, g] - z_root[b, r]) < delta * max(1.0, abs(z_root[b, r]))
+                near += 1
+    # tree
+    tt = oracle.tree_tables(inp.choices)
+    root = npi(step.root)
+    tok_o, pos_o = oracle.tree_tokens(tt, root, ids, npi(inp.kv_len))
+    assert np.array_equal(npi(step.tokens), tok_o)
+    assert np.array_equal(npi(step.positions), pos_o)
+    cand = npi(step.candidates)
+    for p, leaf in enumerate(tt.leaves):
+        chain = tt.ancestors[leaf] + [leaf]
+        want = np.full(tt.dmax + 1, -1)
+        for b in range(wl.B):
+            want[: len(chain)] = tok_o[b, chain]
+            assert cand[b, p].tolist() == want.tolist()
+    # attention
+    a_o = oracle.tree_attention(o["q"], o["k_new"], o["v_new"], o["k_cache"], o["v_cache"], npi(inp.kv_len), tt,
+                                1.0 / math.sqrt(wl.D))
+    assert rel_err(step.attn_out, a_o) < tol
+    # verification logits + acceptance
+    zv = oracle.verify_logits(o["X"], o["lm_head"])
+    assert rel_err(step.logits, zv) < tol
+    near += accept_parity(step, zv, npi(step.tokens), tt, temperature, wl.posterior_threshold,
+                          wl.posterior_alpha, delta, kind)
+    if temperature > 0:
+        H_o = np.array([[oracle.node_posterior(zv[b, i], 0, temperature, 0.09, 0.3)["H"] for i in range(tt.T)]
+                        for b in range(wl.B)])
+        assert rel_err(step.node_H, H_o) < max(tol, 1e-3)
+    # commit (bit-exact on the GPU's own decision)
+    kc_o, vc_o, kl_o, st_o = oracle.kv_commit(o["k_cache"], o["v_cache"], npi(inp.kv_len), o["k_new"],
+                                              o["v_new"], tt, npi(step.best_node))
+    assert np.array_equal(npi(kl), kl_o)
+    assert np.array_equal(np64(kc), kc_o) and np.array_equal(np64(vc), vc_o)
+    st = npi(step.dev_status)
+    assert np.array_equal(st & 1, st_o), st
+    assert np.all((st & ~1) == 0), st
+    return near
+
+
+# ----------------------------------------------------------------------------- generator
+
+
+def test_generator_bit_identical_on_gpu():
+    seed = synth.tensor_seed(7, 3)
+    for dt in (torch.float32, torch.bfloat16):
+        a = synth.normal((3, 1000, 37), seed, 0.02, dt, "cpu")
+        b = synth.normal((3, 1000, 37), seed, 0.02, dt, "cuda").cpu()
+        assert torch.equal(a.view(torch.int16 if dt == torch.bfloat16 else torch.int32),
+                           b.view(torch.int16 if dt == torch.bfloat16 else torch.int32))
+
+
+# ----------------------------------------------------------------------------- tiny (fp32)
+
+@pytest.mark.parametrize("variant", ["random", "plant", "zeroinit"])
+@pytest.mark.parametrize("temperature", [0.0, 0.7])
+def test_tiny_full_step(mb, variant, temperature):
+    wl = synth.WORKLOADS["tiny"]
+    inp = synth.make_inputs(wl, "cuda", variant=variant, plant_depth=2)
+    step, kc, vc, kl = run_step(mb, wl, inp, temperature)
+    near = check_full(wl, inp, step, kc, vc, kl, temperature)
+    assert near <= 2
+    if variant == "plant":
+        assert int(step.accept_len[0]) == 2
+
+
+def test_tiny_root_from_lm_head(mb):
+    wl = synth.WORKLOADS["tiny"]
+    inp = synth.make_inputs(wl, "cuda")
+    step, kc, vc, kl = run_step(mb, wl, inp, 0.7, root_from_lm=True)
+    check_full(wl, inp, step, kc, vc, kl, 0.7, root_from_lm=True)
+
+
+@pytest.mark.parametrize("name", ["tiny", "vicuna7b"])
+def test_zero_init_heads_bitwise(mb, name):
+    """Ultralytics "Medusa Heads" example: with zero FC weights and W2 = lm_head every head
+    reproduces lm_head(h) exactly -- on the GPU: every head's logits are bitwise identical, and
+    each head's top-1 is the root the lm_head path picks."""
+    wl = synth.WORKLOADS[name]
+    inp = synth.make_inputs(wl, "cuda", variant="zeroinit")
+    step = make_step(mb, wl, inp, root_from_lm=True)
+    step.heads(inp.h, inp.W1, inp.b1, inp.W2, inp.lm_head)
+    torch.cuda.synchronize()
+    hl = step.head_logits
+    for k in range(1, wl.K):
+        assert torch.equal(hl[:, k], hl[:, 0])
+    assert torch.equal(step.topk_ids[:, :, 0], step.root[:, None].expand(-1, wl.K))
+    o = step_oracle_inputs(inp)
+    z_base = o["h"] @ o["lm_head"].T
+    assert rel_err(hl[:, 0], z_base) < TOL[wl.dtype]
+
+
+# ----------------------------------------------------------------------------- small bf16, multi-tile
+
+SMALL_BF16 = synth.Workload("small_bf16", 11, H=512, V=3001, K=3, Hq=8, Hkv=2, D=128, L=0, B=3, dtype="bf16",
+                            tree=("cartesian", (3, 2, 2)), ragged=(0, 300))
+SMALL_BF16_D64 = dataclasses.replace(SMALL_BF16, name="small_bf16_d64", config_id=12, D=64, Hq=4, Hkv=4,
+                                     tree=("seeded", 40, (8, 4, 2)), ragged=(60, 200), B=2, V=2048)
+
+
+@pytest.mark.parametrize("wl", [SMALL_BF16, SMALL_BF16_D64], ids=lambda w: w.name)
+@pytest.mark.parametrize("temperature", [0.0, 0.7])
+@pytest.mark.parametrize("variant", ["random", "plant"])
+def test_small_bf16_full_step(mb, wl, temperature, variant):
+    """Ragged kv lengths (including 0), a vocabulary that is not a multiple of any tile,
+    GQA, several requests, both head dims."""
+    inp = synth.make_inputs(wl, "cuda", variant=variant)
+    step, kc, vc, kl = run_step(mb, wl, inp, temperature)
+    near = check_full(wl, inp, step, kc, vc, kl, temperature)
+    assert near <= 3
+
+
+def test_root_only_tree(mb):
+    """Degenerate tree without candidates: only the root is emitted, accept_length 0."""
+    wl = dataclasses.replace(synth.WORKLOADS["tiny"], name="root_only", tree=("cartesian", ()))
+    inp = synth.make_inputs(wl, "cuda")
+    assert inp.choices == [] and inp.T == 1
+    step, kc, vc, kl = run_step(mb, wl, inp, 0.7)
+    assert int(step.accept_len[0]) == 0 and int(step.best_node[0]) == 0
+    assert int(kl[0]) == wl.L + 1
+    check_full(wl, inp, step, kc, vc, kl, 0.7)
+
+
+def test_kv_overflow_flag_leaves_cache(mb):
+    wl = dataclasses.replace(synth.WORKLOADS["tiny"], name="overflow", lmax_slack=1)
+    inp = synth.make_inputs(wl, "cuda", variant="plant", plant_depth=2)
+    step, kc, vc, kl = run_step(mb, wl, inp, 0.7)
+    assert int(step.accept_len[0]) == 2
+    assert int(step.dev_status[0]) & mb.DEV_KV_OVERFLOW
+    assert int(kl[0]) == wl.L
+    assert torch.equal(kc, inp.k_cache) and torch.equal(vc, inp.v_cache)
+
+
+# ----------------------------------------------------------------------------- 7B shape, full size
+
+@pytest.mark.parametrize("temperature", [0.0, 0.7])
+@pytest.mark.parametrize("variant", ["plant", "random"])
+def test_vicuna7b_full_step(mb, temperature, variant):
+    wl = synth.WORKLOADS["vicuna7b"]
+    inp = synth.make_inputs(wl, "cuda", variant=variant)
+    step, kc, vc, kl = run_step(mb, wl, inp, temperature, kv_len_hint=wl.L)
+    near = check_full(wl, inp, step, kc, vc, kl, temperature)
+    assert near <= 3
+    if variant == "plant":
+        assert int(step.accept_len[0]) >= inp.plant["depths"][0]
