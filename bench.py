@@ -1,0 +1,407 @@
+#!/usr/bin/env python
+"""Medusa decode-step benchmark: verifies/s at the Vicuna-7B shape on one B300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+A step is one pass of the whole hot path over one batch: Medusa heads + top-k,
+tree expansion, tree attention over KV cache + tree, lm_head verification with
+typical acceptance, KV commit of the accepted path.  One "verify" is one
+request's step (a step processes B requests).  Inputs are seeded synthetic
+tensors of the workload's shapes (random-init weights), resident in HBM.
+The per-step working set (1.79 GB at the 7B shape) exceeds the 126 MB L2, so
+no flush is added between steps.  Under torchrun every rank runs an
+independent replica (weak scaling); rank 0 prints one JSON line.
+
+--impl reference times the CPU oracle (fp64 numpy, test infrastructure) on
+the host cores, on bounded samples of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "Medusa decode-step verifies/sec at 7B shape; % of HBM/tensor roofline"
+UNIT = "verifies/s"
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="vicuna7b")
+    ap.add_argument("--temperature", type=float, default=0.7)
+    ap.add_argument("--unroll", type=int, default=20, help="steps per captured CUDA graph")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget-s", type=float, default=30.0)
+    return ap.parse_args()
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+# ----------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while the timed region runs."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- roofline bookkeeping
+
+def step_bytes(wl, T):
+    """Algorithmic bytes of each stage of one step (weights + KV + activations + outputs)."""
+    es = 2 if wl.dtype == "bf16" else 4
+    B, H, V, K, Hq, Hkv, D = wl.B, wl.H, wl.V, wl.K, wl.Hq, wl.Hkv, wl.D
+    L = sum(wl.kv_lens())
+    heads = es * (K * H * H + K * H + K * V * H + B * H) + B * K * H * es * 2
+    attn = es * (2 * L * Hkv * D + B * T * Hq * D + 2 * B * T * Hkv * D) + 4 * B * T * Hq * D
+    verify = es * (V * H + B * T * H) + 4 * B * T
+    return {"heads": heads, "attention": attn, "verify": verify}
+
+
+def traffic_from_profile(kernel_key: str):
+    """DRAM bytes per launch recorded from an ncu capture, if the kernel source is unchanged since."""
+    path = os.path.join(ROOT, "profiles", f"{kernel_key}.md")
+    if not os.path.exists(path):
+        return None
+    txt = open(path).read()
+    m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", txt)
+    s = re.search(r"source_sha256:\s*([0-9a-f]+)", txt)
+    src = re.search(r"source_file:\s*(\S+)", txt)
+    if not (m and s and src):
+        return None
+    cur = hashlib.sha256(open(os.path.join(ROOT, src.group(1)), "rb").read()).hexdigest()
+    return float(m.group(1)) if cur.startswith(s.group(1)) else None
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return d.get("hbm_gbs", 6400.0), d.get("bf16_tflops", 1800.0), "measured"
+    return 6400.0, 1800.0, "fallback"
+
+
+# ----------------------------------------------------------------------------- our arm
+
+def run_ours(args, ws, rank, local):
+    import torch
+    import torch.distributed as dist
+
+    import medusa_head_speculative_04_b300 as mb
+    import synth
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    wl = synth.WORKLOADS[args.workload]
+    inp = synth.make_inputs(wl, dev, variant="plant")
+    T = inp.T
+    step = mb.MedusaStep(inp.choices, wl.B, wl.H, wl.V, wl.K, wl.Hq, wl.Hkv, wl.D, wl.Lmax, wl.k_needed(),
+                         inp.dtype, device=dev, kv_len_hint=max(wl.kv_lens()), keep_node_stats=False)
+    kc, vc = inp.k_cache.clone(), inp.v_cache.clone()
+    kv_len0 = inp.kv_len.clone()
+    kl = kv_len0.clone()
+    root = inp.root.clone()
+    tau = args.temperature
+    s = torch.cuda.Stream(dev)
+
+    ev_pairs = []
+
+    def one_step(timed_events=False):
+        kl.copy_(kv_len0)                       # every step starts from the same prefix
+        step.root.copy_(root)
+        if timed_events:
+            e = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(4)]
+            e[0].record()
+        step.heads(inp.h, inp.W1, inp.b1, inp.W2)
+        if timed_events:
+            e[1].record()
+        step.build(kl)
+        step.attention(inp.q, inp.k_new, inp.v_new, kc, vc, kl)
+        if timed_events:
+            e[2].record()
+        step.verify(inp.X, inp.lm_head, tau, wl.posterior_threshold, wl.posterior_alpha)
+        if timed_events:
+            e[3].record()
+        step.commit(inp.k_new, inp.v_new, kc, vc, kl)
+        if timed_events:
+            ev_pairs.append(e)
+
+    # eager warm-up (function attributes, tensor maps), then graphs
+    with torch.cuda.stream(s):
+        one_step()
+    torch.cuda.synchronize()
+    n0 = mb.kernel_launches()
+    g1 = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g1, stream=s):
+        one_step()
+    launches_per_step = mb.kernel_launches() - n0
+    S = max(1, min(args.unroll, args.steps))
+    gS = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gS, stream=s):
+        for _ in range(S):
+            one_step(timed_events=True)
+    reps, rem = divmod(args.steps, S)
+
+    for _ in range(max(3, args.warmup)):
+        g1.replay()
+    torch.cuda.synchronize()
+    if ws > 1:
+        dist.barrier()
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    if ws > 1:
+        dist.barrier()
+    with torch.cuda.stream(s):
+        start.record()
+        for _ in range(reps):
+            gS.replay()
+        for _ in range(rem):
+            g1.replay()
+        end.record()
+    torch.cuda.synchronize()
+    if ws > 1:
+        dist.barrier()
+    clocks = sampler.stop()
+    ms = start.elapsed_time(end)
+    t = torch.tensor([ms], device=dev)
+    if ws > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    ms_max = float(t.item())
+    status = int(step.dev_status.max().item())
+
+    stage_ms = {"heads": [], "attention": [], "verify": []}
+    if reps > 0:
+        for e in ev_pairs:
+            stage_ms["heads"].append(e[0].elapsed_time(e[1]))
+            stage_ms["attention"].append(e[1].elapsed_time(e[2]))
+            stage_ms["verify"].append(e[2].elapsed_time(e[3]))
+
+    # end-to-end through the public API: pinned host inputs in, results out, every step
+    pin = lambda x: x.detach().cpu().pin_memory()
+    host_in = {k: pin(getattr(inp, k)) for k in ("h", "X", "q", "k_new", "v_new")}
+    host_root = pin(root)
+    dev_in = {k: torch.empty_like(getattr(inp, k)) for k in host_in}
+    outs = (step.accept_len, step.accepted_tokens, step.next_root, step.best_node)
+    host_out = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs]
+    h2d = sum(v.numel() * v.element_size() for v in host_in.values()) + host_root.numel() * 4
+    d2h = sum(o.numel() * o.element_size() for o in outs)
+    e2e_steps = max(10, min(args.steps, 500))
+
+    def e2e_step():
+        for k, v in host_in.items():
+            dev_in[k].copy_(v, non_blocking=True)
+        step.root.copy_(host_root, non_blocking=True)
+        kl.copy_(kv_len0)
+        step.run(dev_in["h"], inp.W1, inp.b1, inp.W2, inp.lm_head, dev_in["X"], dev_in["q"], dev_in["k_new"],
+                 dev_in["v_new"], kc, vc, kl, tau, wl.posterior_threshold, wl.posterior_alpha)
+        for o, ho in zip(outs, host_out):
+            ho.copy_(o, non_blocking=True)
+
+    with torch.cuda.stream(s):
+        for _ in range(3):
+            e2e_step()
+    torch.cuda.synchronize()
+    if ws > 1:
+        dist.barrier()
+    with torch.cuda.stream(s):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(e2e_steps):
+            e2e_step()
+        e1.record()
+    torch.cuda.synchronize()
+    te = torch.tensor([e0.elapsed_time(e1)], device=dev)
+    if ws > 1:
+        dist.all_reduce(te, op=dist.ReduceOp.MAX)
+    e2e_value = e2e_steps * wl.B * ws / (float(te.item()) / 1e3)
+
+    if rank != 0:
+        return None
+
+    value = args.steps * wl.B * ws / (ms_max / 1e3)
+    sb = step_bytes(wl, T)
+    hbm, bf16, src = measured_peaks()
+    heads_ms = statistics.mean(stage_ms["heads"]) if stage_ms["heads"] else None
+    roof = None
+    if heads_ms:
+        ach = sb["heads"] / (heads_ms / 1e3) / 1e9
+        roof = {"kernel": "medusa_heads_topk (heads_fc + heads_vocab_topk)", "bound": "hbm",
+                "achieved": round(ach, 1), "peak": hbm, "unit": "GB/s", "frac": round(ach / hbm, 4),
+                "peak_source": src, "algorithmic_bytes": sb["heads"],
+                "traffic": traffic_from_profile("heads_vicuna7b")}
+    stages = {}
+    for k, v in stage_ms.items():
+        if v:
+            m = statistics.mean(v)
+            stages[k] = {"ms": round(m, 4), "GB/s": round(sb[k] / (m / 1e3) / 1e9, 1),
+                         "frac_hbm": round(sb[k] / (m / 1e3) / 1e9 / hbm, 4)}
+    total_bytes = sum(sb.values())
+    ms_step = ms_max / args.steps
+    out = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+        "warmup": max(3, args.warmup), "ms_per_step": round(ms_step, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic (seeded, random-init weights)",
+        "config": {"workload": wl.name, "batch": wl.B, "hidden": wl.H, "vocab": wl.V, "heads": wl.K,
+                   "tree_nodes": T, "q_heads": wl.Hq, "kv_heads": wl.Hkv, "head_dim": wl.D, "kv_len": wl.L,
+                   "temperature": tau, "inputs": "planted accept path", "parallelism": f"replicas x{ws}",
+                   "l2": "per-step working set %.2f GB > 126 MB L2; no flush" % (total_bytes / 1e9),
+                   "timing": f"CUDA graphs of {S} steps, CUDA events"},
+        "roofline": roof,
+        "step_roofline": {"bytes": total_bytes, "frac_hbm": round(total_bytes / (ms_step / 1e3) / 1e9 / hbm, 4)},
+        "stages": stages,
+        "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "note": "eager calls through MedusaStep.run with pinned host inputs/outputs"},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks,
+        "dev_status": status,
+    }
+    return out, inp, wl
+
+
+# ----------------------------------------------------------------------------- oracle timing
+
+def oracle_sample(wl, inp, temperature, budget_s, max_steps):
+    """Time the CPU oracle on full decode steps of the workload (fp64 numpy).
+
+    ``inp`` holds the step's seeded inputs (on any device); they are copied to
+    host fp64 arrays before the clock starts."""
+    import numpy as np
+    import torch
+    import oracle
+    try:
+        from threadpoolctl import threadpool_info
+        cores = max([d.get("num_threads", 1) for d in threadpool_info()] or [os.cpu_count()])
+    except Exception:
+        cores = os.cpu_count()
+    f = lambda t: t.detach().to("cpu", torch.float64).numpy()
+    args = [f(inp.h), f(inp.W1), f(inp.b1), f(inp.W2), f(inp.lm_head), f(inp.X), f(inp.q), f(inp.k_new),
+            f(inp.v_new), f(inp.k_cache), f(inp.v_cache), inp.kv_len.cpu().numpy()]
+    root = inp.root.cpu().numpy()
+    times = []
+    t_all = time.perf_counter()
+    while len(times) < max_steps:
+        t0 = time.perf_counter()
+        oracle.run_step(*args, inp.choices, wl.k_needed(), temperature, wl.posterior_threshold,
+                        wl.posterior_alpha, root=root, u_bf16=(wl.dtype == "bf16"))
+        times.append(time.perf_counter() - t0)
+        if time.perf_counter() - t_all > budget_s:
+            break
+    per = sum(times) / len(times)
+    return {"value": round(wl.B / per, 4), "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{len(times)} full decode step(s) of {wl.name} (B={wl.B}), fp64 numpy, "
+                      f"{per:.2f} s/step"}, len(times), per
+
+
+def run_reference(args, ws, rank):
+    if rank != 0:
+        return None
+    import torch
+    import synth
+    wl = synth.WORKLOADS[args.workload]
+    # inputs come from the seeded generator (on a GPU when there is one, as it is much
+    # faster there); the oracle only ever sees host copies
+    gen_dev = "cuda" if torch.cuda.is_available() else "cpu"
+    inp = synth.make_inputs(wl, gen_dev, variant="plant")
+    cb, n, per = oracle_sample(wl, inp, args.temperature, args.cpu_budget_s * 4, max(1, args.steps))
+    return {"impl": "reference", "metric": METRIC, "value": cb["value"], "unit": UNIT, "n_gpus": ws,
+            "steps": n, "warmup": 0, "ms_per_step": round(per * 1e3, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
+            "config": {"workload": wl.name, "batch": wl.B, "temperature": args.temperature},
+            "cpu_baseline": cb,
+            "e2e": {"value": cb["value"], "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    args = parse_args()
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        backend = "nccl" if args.impl == "ours" else "gloo"
+        dist.init_process_group(backend)
+    if args.impl == "reference":
+        out = run_reference(args, ws, rank)
+        if out:
+            print(json.dumps(out))
+        return
+    res = run_ours(args, ws, rank, local)
+    if res is None:
+        return
+    out, inp, wl = res
+    if not args.no_cpu_baseline and rank == 0 and ws == 1:
+        cb, _, _ = oracle_sample(wl, inp, args.temperature, args.cpu_budget_s, 3)
+        out["cpu_baseline"] = cb
+    else:
+        out["cpu_baseline"] = None
+    print(json.dumps(out))
+
+
+if __name__ == "__main__":
+    main()

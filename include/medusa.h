@@ -71,6 +71,10 @@ typedef enum { MEDUSA_F32 = 0, MEDUSA_BF16 = 1 } medusa_dtype;
 
 const char* medusa_status_string(int status);
 
+/* Number of kernels this library has launched (or recorded into a stream
+ * capture) in this process so far; a diagnostic for counting launches. */
+uint64_t medusa_kernel_launches(void);
+
 /* ------------------------------------------------------------------------
  * Candidate tree ("medusa_choices").
  * A fixed tree is given as a list of rank tuples: choice (r1..rd) is the

@@ -58,6 +58,7 @@ def _sig(name, restype, argtypes):
 
 
 _sig("medusa_status_string", ctypes.c_char_p, [ctypes.c_int])
+_sig("medusa_kernel_launches", ctypes.c_uint64, [])
 _sig("medusa_tree_create", ctypes.c_int, [_vp, _vp, _i32, ctypes.POINTER(_vp)])
 _sig("medusa_tree_get_info", ctypes.c_int, [_vp, ctypes.POINTER(TreeInfo)])
 _sig("medusa_tree_copy_tables", ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp])
@@ -145,6 +146,11 @@ class Tree:
             self.close()
         except Exception:
             pass
+
+
+def kernel_launches() -> int:
+    """Kernels launched (or captured) by the library in this process so far."""
+    return int(lib.medusa_kernel_launches())
 
 
 def workspace(nbytes: int, device) -> torch.Tensor:

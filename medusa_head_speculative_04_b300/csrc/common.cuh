@@ -97,13 +97,17 @@ __device__ inline uint64_t globaltimer_ns() {
 // Bounded-wait limit for every device-side spin (about one second).
 constexpr uint64_t kSpinLimitNs = 1000000000ull;
 
+// Process-wide count of kernels this library has launched (or captured).
+void note_launch();
+
 }  // namespace medusa
 
-// Host-side launch error check used by every entry point.
+// Host-side check after every kernel launch of an entry point.
 #define MEDUSA_LAUNCH_CHECK()                                  \
   do {                                                         \
     if (cudaPeekAtLastError() != cudaSuccess) {                \
       (void)cudaGetLastError();                                \
       return MEDUSA_ERR_CUDA;                                  \
     }                                                          \
+    medusa::note_launch();                                     \
   } while (0)

@@ -7,6 +7,7 @@
 // under every branch (Ultralytics glossary "Medusa Heads", section "Tree
 // attention and accepting tokens").
 #include <algorithm>
+#include <atomic>
 #include <cstring>
 #include <map>
 #include <vector>
@@ -14,6 +15,13 @@
 #include "tree.cuh"
 
 using namespace medusa;
+
+namespace medusa {
+static std::atomic<uint64_t> g_launches{0};
+void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+}  // namespace medusa
+
+MEDUSA_API uint64_t medusa_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
 
 MEDUSA_API const char* medusa_status_string(int s) {
   switch (s) {
