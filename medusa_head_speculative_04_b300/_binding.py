@@ -36,7 +36,7 @@ def _load() -> ctypes.CDLL:
     if not os.path.exists(_LIB_PATH):
         raise ImportError(
             f"{_LIB_PATH} is missing: build the CUDA library first "
-            "(python -m medusa_head_speculative_04_b300.build)")
+            "(python medusa_head_speculative_04_b300/build.py)")
     return ctypes.CDLL(_LIB_PATH)
 
 

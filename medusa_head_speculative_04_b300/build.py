@@ -1,6 +1,6 @@
 """Build the CUDA library (libmedusa_b300.so) in-tree for sm_103a.
 
-    python -m medusa_head_speculative_04_b300.build [--verbose-ptxas]
+    python medusa_head_speculative_04_b300/build.py [--verbose-ptxas]
 
 Compiles every csrc/*.cu with nvcc into one shared object next to this file.
 The library links the CUDA runtime statically and reaches the driver's

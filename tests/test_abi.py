@@ -13,8 +13,8 @@ HEADER = os.path.join(ROOT, "include", "medusa.h")
 
 @pytest.fixture(scope="module")
 def lib():
-    from medusa_head_speculative_04_b300 import build
-    build.build()
+    import __graft_entry__
+    __graft_entry__._builder().build()
     import medusa_head_speculative_04_b300 as m
     return m
 
