@@ -53,7 +53,8 @@ typedef enum {
   MEDUSA_ERR_ALIGNMENT = -2,   /* a device pointer is not 16-byte aligned      */
   MEDUSA_ERR_UNSUPPORTED = -3, /* shape outside what the kernels implement      */
   MEDUSA_ERR_WORKSPACE = -4,   /* ws missing or smaller than *_workspace_size   */
-  MEDUSA_ERR_CUDA = -5         /* a CUDA call or kernel launch failed           */
+  MEDUSA_ERR_CUDA = -5,        /* a CUDA call or kernel launch failed           */
+  MEDUSA_ERR_SCRATCH_LIMIT = -6 /* shape needs more than the built-in scratch   */
 } medusa_status;
 
 /* bits OR-ed into dev_status[b] */
@@ -135,6 +136,32 @@ int medusa_heads_topk(const void* h, const void* w1, const void* b1, const void*
                       int32_t topk, medusa_dtype dtype, float* head_logits, int32_t* topk_ids,
                       float* topk_vals, int32_t* root_tok, void* ws, size_t ws_bytes,
                       medusa_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * medusa_heads_topk_noalloc
+ * No counterpart on the source pages: a convenience of this library.
+ * Same computation, arguments and outputs as medusa_heads_topk, minus the
+ * workspace, for callers that cannot allocate device memory -- cudaMalloc may
+ * synchronise the device and takes a driver-wide lock, so latency-bound decode
+ * loops, plugins living inside another framework's memory pool and programs
+ * with a fixed device-memory budget often may not call it.  The scratch is a
+ * fixed array of MEDUSA_NOALLOC_SCRATCH_BYTES compiled into the library; every
+ * GPU that loads the library holds it until the process exits.
+ *   - Shapes whose scratch would exceed that size return
+ *     MEDUSA_ERR_SCRATCH_LIMIT (about B*K*H*elem + 8*(K+1)*B*topk*CTAs per head
+ *     bytes; the Llama-8B shape at batch 16 needs about 1.5 MB).
+ *   - The first call on each device looks up the array's device address (with
+ *     that device current); make that first call before any stream capture.
+ *   - All calls share the one array and it keeps the last call's contents;
+ *     the ticket counters are cleared on the stream at every call.  Calls
+ *     that overlap on the GPU (other streams, other host threads) race.
+ *   - Allocates nothing: no cudaMalloc/cudaFree, no allocating library routine.
+ * ---------------------------------------------------------------------- */
+#define MEDUSA_NOALLOC_SCRATCH_BYTES (8u << 20)
+int medusa_heads_topk_noalloc(const void* h, const void* w1, const void* b1, const void* w2,
+                              const void* lm_head, int32_t B, int32_t H, int32_t V, int32_t K,
+                              int32_t topk, medusa_dtype dtype, float* head_logits, int32_t* topk_ids,
+                              float* topk_vals, int32_t* root_tok, medusa_stream_t stream);
 
 /* ------------------------------------------------------------------------
  * medusa_build_tree

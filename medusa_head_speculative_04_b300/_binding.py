@@ -66,6 +66,8 @@ _sig("medusa_tree_destroy", None, [_vp])
 _sig("medusa_heads_topk_workspace_size", _sz, [_i32, _i32, _i32, _i32, _i32, _i32, ctypes.c_int])
 _sig("medusa_heads_topk", ctypes.c_int,
      [_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, ctypes.c_int, _vp, _vp, _vp, _vp, _vp, _sz, _vp])
+_sig("medusa_heads_topk_noalloc", ctypes.c_int,
+     [_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, ctypes.c_int, _vp, _vp, _vp, _vp, _vp])
 _sig("medusa_build_tree", ctypes.c_int, [_vp, _vp, _vp, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _vp])
 _sig("medusa_tree_attention_workspace_size", _sz, [_vp, _i32, _i32, _i32, _i32, _i32, _i32, ctypes.c_int])
 _sig("medusa_tree_attention", ctypes.c_int,
@@ -170,6 +172,17 @@ def medusa_heads_topk(h, w1, b1, w2, lm_head, topk: int, topk_ids, topk_vals, ro
         _ptr(h), _ptr(w1), _ptr(b1), _ptr(w2), _ptr(lm_head), B, H, V, K, topk, dtype_code(h),
         _ptr(head_logits), _ptr(topk_ids), _ptr(topk_vals), _ptr(root_tok), _ptr(ws), ws.numel(),
         _stream(stream)))
+
+
+def medusa_heads_topk_noalloc(h, w1, b1, w2, lm_head, topk: int, topk_ids, topk_vals, root_tok,
+                              head_logits=None, stream=None) -> None:
+    """medusa_heads_topk without a workspace, for callers that cannot allocate device memory
+    (the scratch is a fixed array inside the library, shared by every call)."""
+    B, H = h.shape
+    K, V = w2.shape[0], w2.shape[1]
+    _check("medusa_heads_topk_noalloc", lib.medusa_heads_topk_noalloc(
+        _ptr(h), _ptr(w1), _ptr(b1), _ptr(w2), _ptr(lm_head), B, H, V, K, topk, dtype_code(h),
+        _ptr(head_logits), _ptr(topk_ids), _ptr(topk_vals), _ptr(root_tok), _stream(stream)))
 
 
 def medusa_build_tree(tree: Tree, root_tok, topk_ids, kv_len, tree_tokens, position_ids,

@@ -12,6 +12,7 @@
 // activations).  K2 fuses the top-k: every CTA keeps the top-k of its slice of
 // the vocabulary, and the last CTA of a head (ticket counter) merges them.
 #include <algorithm>
+#include <mutex>
 
 #include "gemv.cuh"
 
@@ -271,6 +272,80 @@ MEDUSA_API int medusa_heads_topk(const void* h, const void* w1, const void* b1, 
   HeadsWs w = carve_heads_ws(ws, p, B, H, K, topk, es);
   if (!ws || ws_bytes < w.bytes) return MEDUSA_ERR_WORKSPACE;
   auto st = reinterpret_cast<cudaStream_t>(stream);
+  if (dtype == MEDUSA_BF16)
+    return heads_dispatch(p, w, static_cast<const __nv_bfloat16*>(h), static_cast<const __nv_bfloat16*>(w1),
+                          static_cast<const __nv_bfloat16*>(b1), static_cast<const __nv_bfloat16*>(w2),
+                          static_cast<const __nv_bfloat16*>(lm_head), B, H, V, K, topk, head_logits, topk_ids,
+                          topk_vals, root_tok, st);
+  return heads_dispatch(p, w, static_cast<const float*>(h), static_cast<const float*>(w1),
+                        static_cast<const float*>(b1), static_cast<const float*>(w2),
+                        static_cast<const float*>(lm_head), B, H, V, K, topk, head_logits, topk_ids, topk_vals,
+                        root_tok, st);
+}
+
+// ---------------------------------------------------------------------------
+// medusa_heads_topk_noalloc: the same heads step for callers that must not
+// allocate device memory.  Its scratch (u, per-CTA candidates, tickets) is a
+// fixed array compiled into this library, so the caller passes only inputs
+// and outputs.  The array lives on every GPU that loads the library until the
+// process exits, and all calls share it: calls that overlap on the GPU race.
+// ---------------------------------------------------------------------------
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = static_cast<size_t>(MEDUSA_NOALLOC_SCRATCH_BYTES);
+constexpr int kMaxDevices = 64;
+
+static __device__ __align__(256) unsigned char g_heads_scratch[kNoAllocScratchBytes];
+
+// Device address of g_heads_scratch on the current device.  Host code only has
+// a host-side stand-in under that name, so the address is looked up once per
+// device (with that device current) and cached.
+int heads_scratch_address(void** out) {
+  static std::mutex mu;
+  static void* addr[kMaxDevices] = {};
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MEDUSA_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_heads_scratch) != cudaSuccess || !p) {
+      (void)cudaGetLastError();
+      return MEDUSA_ERR_CUDA;
+    }
+    addr[dev] = p;
+  }
+  *out = addr[dev];
+  return MEDUSA_OK;
+}
+
+}  // namespace
+
+MEDUSA_API int medusa_heads_topk_noalloc(const void* h, const void* w1, const void* b1, const void* w2,
+                                         const void* lm_head, int32_t B, int32_t H, int32_t V, int32_t K,
+                                         int32_t topk, medusa_dtype dtype, float* head_logits, int32_t* topk_ids,
+                                         float* topk_vals, int32_t* root_tok, medusa_stream_t stream) {
+  if (!h || !w1 || !b1 || !w2 || !topk_ids || !topk_vals || !root_tok) return MEDUSA_ERR_INVALID_ARG;
+  if (dtype != MEDUSA_F32 && dtype != MEDUSA_BF16) return MEDUSA_ERR_INVALID_ARG;
+  if (B < 1 || B > MEDUSA_MAX_BATCH || K < 1 || V < 1 || H < 8 || topk < 1 || topk > MEDUSA_MAX_TOPK || topk > V)
+    return MEDUSA_ERR_INVALID_ARG;
+  if (H % 8 != 0) return MEDUSA_ERR_UNSUPPORTED;
+  const void* ptrs[] = {h, w1, b1, w2, topk_ids, topk_vals, root_tok};
+  for (const void* q : ptrs)
+    if (!aligned16(q)) return MEDUSA_ERR_ALIGNMENT;
+  if ((lm_head && !aligned16(lm_head)) || (head_logits && !aligned16(head_logits))) return MEDUSA_ERR_ALIGNMENT;
+  const int es = dtype == MEDUSA_BF16 ? 2 : 4;
+  HeadsPlan p = plan_heads(B, H, V, K, lm_head != nullptr, es);
+  if (carve_heads_ws(nullptr, p, B, H, K, topk, es).bytes > kNoAllocScratchBytes) return MEDUSA_ERR_SCRATCH_LIMIT;
+  void* scratch = nullptr;
+  const int rc = heads_scratch_address(&scratch);
+  if (rc != MEDUSA_OK) return rc;
+  HeadsWs w = carve_heads_ws(scratch, p, B, H, K, topk, es);
+  auto st = reinterpret_cast<cudaStream_t>(stream);
+  // the ticket counters must start at zero whatever an earlier call left behind
+  if (cudaMemsetAsync(w.counters, 0, static_cast<size_t>(p.nblk) * sizeof(int), st) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return MEDUSA_ERR_CUDA;
+  }
   if (dtype == MEDUSA_BF16)
     return heads_dispatch(p, w, static_cast<const __nv_bfloat16*>(h), static_cast<const __nv_bfloat16*>(w1),
                           static_cast<const __nv_bfloat16*>(b1), static_cast<const __nv_bfloat16*>(w2),

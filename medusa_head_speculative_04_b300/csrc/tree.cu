@@ -31,6 +31,7 @@ MEDUSA_API const char* medusa_status_string(int s) {
     case MEDUSA_ERR_UNSUPPORTED: return "unsupported shape";
     case MEDUSA_ERR_WORKSPACE: return "workspace missing or too small";
     case MEDUSA_ERR_CUDA: return "CUDA call or launch failed";
+    case MEDUSA_ERR_SCRATCH_LIMIT: return "shape needs more scratch than the built-in array holds";
     default: return "unknown status";
   }
 }
