@@ -9,60 +9,101 @@
 // candidate tokens enter one forward pass and the mask lets each token see
 // only its ancestors.
 //
-// bf16 path: split-KV ("flash-decoding") over the cache plus one extra split
-// for the tree segment, where the cached ancestor bitmask masks the scores.
-// One CTA owns a tile of up to 128 query rows of one KV head: a query row is
-// (node, query head of this KV head's group), so the heads that share a KV
-// head share every K/V tile load.  K/V tiles are staged in shared memory by
-// cp.async (double buffered), QK^T and PV run on mma.sync bf16 tensor-core
-// tiles with fp32 accumulation and an fp32 online softmax.  A second kernel
-// merges the splits.  fp32 path: an exact scalar kernel (small shapes).
+// bf16 path: one persistent-style launch over a balanced split of all key
+// tiles.  The work of a request's KV head is a sequence of 64-key tiles: the
+// kv_len cached keys, then the tree's own keys (masked by the cached ancestor
+// bitmask; tiles no query row of the tile can see are skipped).  Every CTA
+// takes an equal share of the concatenated tile sequence of all requests and
+// heads, computed on the device from kv_len, so ragged batches stay balanced.
+// A query tile holds up to 128 rows (node, query head of the KV head's group):
+// heads that share a KV head share every K/V tile.  One producer warp streams
+// K/V tiles into shared memory with TMA (128-byte swizzled boxes, mbarrier
+// completion, kStages deep); each consumer warp owns 16 query rows and runs
+// QK^T and PV on mma.sync bf16 tiles with an fp32 online softmax.  A head
+// whose tiles all fall to one CTA is written out directly; a head split over
+// several CTAs leaves one partial (unnormalised output, running max and sum)
+// per CTA, and a combine launch merges them (one warp per output row, every
+// partial's loads in flight at once).
+// fp32 path: an exact scalar kernel (small shapes).
 #include <algorithm>
 
+#include "tc.cuh"
 #include "tree.cuh"
 
 using namespace medusa;
 
 namespace {
 
-constexpr int KB = 64;  // keys per smem tile
+constexpr int KB = 64;          // keys per tile
+constexpr int kStages = 3;      // K/V tiles in flight per CTA
+constexpr int kCtasPerSm = 2;
+constexpr int kMaxWarps = 8;    // consumer warps: 128 query rows
 
 struct AttnPlan {
-  int G, R, n_qt, rows_per_tile, nwarps, n_splits, chunk, n_parts, R_pad;
+  int G, R, n_qt, rpt, W, ntt, nctas, units;
 };
 
-AttnPlan plan_attn(int T, int B, int Hq, int Hkv, int Lmax, int hint) {
+AttnPlan plan_attn(int T, int B, int Hq, int Hkv, int Lmax, int hint, int sms) {
   AttnPlan p{};
   p.G = Hq / Hkv;
   p.R = T * p.G;
-  p.n_qt = cdiv(p.R, 128);
-  p.rows_per_tile = cdiv(cdiv(p.R, p.n_qt), 16) * 16;
-  p.nwarps = p.rows_per_tile / 16;
-  p.R_pad = p.n_qt * p.rows_per_tile;
+  p.n_qt = cdiv(p.R, 16 * kMaxWarps);
+  p.rpt = cdiv(cdiv(p.R, p.n_qt), 16) * 16;
+  p.W = p.rpt / 16;
+  p.ntt = cdiv(T, KB);
+  p.units = B * Hkv * p.n_qt;
   const int L = hint > 0 ? std::min(hint, Lmax) : Lmax;
-  const int base = B * Hkv * p.n_qt;
-  const int target = 2 * 148;
-  int ns = std::max(1, (target + base / 2) / base);
-  ns = std::max(ns, cdiv(std::max(L, 1), 1024));
-  ns = std::min(ns, std::max(1, cdiv(std::max(L, 1), KB)));
-  p.chunk = cdiv(cdiv(std::max(L, 1), ns), KB) * KB;
-  p.n_splits = cdiv(std::max(L, 1), p.chunk);
-  p.n_parts = p.n_splits + 1;
+  const long total = static_cast<long>(p.units) * (cdiv(std::max(L, 0), KB) + p.ntt);
+  p.nctas = static_cast<int>(std::max(1L, std::min(static_cast<long>(kCtasPerSm) * sms, total)));
   return p;
 }
 
-size_t attn_ws_bytes(const AttnPlan& p, int B, int Hkv, int D) {
-  const size_t nrow = static_cast<size_t>(B) * Hkv * p.n_parts * p.R_pad;
-  return align_up(nrow * D * 4, 256) + align_up(nrow * 8, 256);
+// Partial results: a CTA's range starts and ends inside at most two split
+// heads, so each CTA owns two slots: slot 0 for the head its range starts in,
+// slot 1 for the head it ends in.
+struct AttnWs {
+  float* o_part;    // [nctas * 2 slots][rpt][D]
+  float2* ml_part;  // [nctas * 2 slots][rpt] (running max, sum)
+  size_t bytes;
+};
+
+AttnWs carve_attn_ws(void* base, const AttnPlan& p, int D) {
+  AttnWs w{};
+  size_t o = 0;
+  auto take = [&](size_t n) { size_t s = o; o = align_up(o + n, 256); return s; };
+  const size_t slots = static_cast<size_t>(p.nctas) * 2 * p.rpt;
+  const size_t oo = take(slots * D * 4), om = take(slots * 8);
+  char* c = static_cast<char*>(base);
+  if (c) {
+    w.o_part = reinterpret_cast<float*>(c + oo);
+    w.ml_part = reinterpret_cast<float2*>(c + om);
+  }
+  w.bytes = o;
+  return w;
 }
+
+int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return 148;
+  }
+  return n;
+}
+
+struct AttnArgs {
+  medusa_tree_dev tr;
+  const __nv_bfloat16* q;
+  const int32_t* kv_len;
+  float* out;
+  AttnWs ws;
+  int32_t* dev_status;
+  int B, T, Hq, Hkv, Lmax;
+  float scale_log2;
+  AttnPlan p;
+};
 
 __device__ inline uint32_t ld_u32(const __nv_bfloat16* p) { return *reinterpret_cast<const uint32_t*>(p); }
-
-__device__ inline void cp_async16(uint32_t dst, const void* src, bool valid) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src), "r"(valid ? 16 : 0));
-}
-__device__ inline void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::); }
-template <int N> __device__ inline void cp_async_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N)); }
 
 __device__ inline void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
@@ -82,255 +123,440 @@ __device__ inline uint32_t pack_bf16(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
-// Swizzled smem tile [KB keys][D]: 16-byte chunk c of key row j sits at c ^ (j & 7).
-template <int D>
+// A K or V tile in shared memory is D/64 TMA boxes of [64 keys][64 elements],
+// each 8 KB, written with the 128-byte swizzle: 16-byte chunk c of key row j
+// of a box sits at chunk position c ^ (j & 7).  `chunk` counts 16-byte chunks
+// across the whole D-element row.
 __device__ inline uint32_t tile_addr(uint32_t base, int key, int chunk) {
-  return base + key * (D * 2) + ((chunk ^ (key & 7)) << 4);
+  return base + ((chunk >> 3) << 13) + key * 128 + (((chunk & 7) ^ (key & 7)) << 4);
 }
 
-template <int D>
-__global__ void __launch_bounds__(256) tree_attn_bf16_kernel(
-    medusa_tree_dev tr, const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k_new,
-    const __nv_bfloat16* __restrict__ v_new, const __nv_bfloat16* __restrict__ k_cache,
-    const __nv_bfloat16* __restrict__ v_cache, const int32_t* __restrict__ kv_len, int Hq, int Hkv, int Lmax,
-    AttnPlan p, float scale_log2, float* __restrict__ o_part, float2* __restrict__ ml_part) {
-  extern __shared__ __align__(128) unsigned char smem[];
-  constexpr int NCH = D / 8;  // 16-byte chunks per row
-  const int part = blockIdx.x, qt = blockIdx.y, zb = blockIdx.z;
-  const int b = zb / Hkv, g = zb % Hkv;
-  const int T = tr.T, G = p.G, R = p.R;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int gq = lane >> 2, tq = lane & 3;
-  const int row0 = qt * p.rows_per_tile + warp * 16;
-  const bool is_tree = part == p.n_splits;
-  const int L = min(max(kv_len[b], 0), Lmax);
+// One (request, KV head, query tile) unit met by a CTA: tiles [t0, t1) of its
+// virtual tile sequence (nc cache tiles, then the tree tiles).
+struct Seg {
+  int b, g, qt, nc, t0, t1;
+  long long ustart, uend;
+};
 
-  const uint32_t sK = smem_u32(smem);
-  const uint32_t sV = sK + 2 * KB * D * 2;
-
-  // query fragments (A operand) for this warp's 16 rows
-  const int ra = row0 + gq, rb = row0 + gq + 8;
-  const int node_a = ra < R ? ra / G : -1, node_b = rb < R ? rb / G : -1;
-  const __nv_bfloat16* qa_ptr = node_a >= 0 ? q + ((static_cast<size_t>(b) * T + node_a) * Hq + g * G + ra % G) * D : nullptr;
-  const __nv_bfloat16* qb_ptr = node_b >= 0 ? q + ((static_cast<size_t>(b) * T + node_b) * Hq + g * G + rb % G) * D : nullptr;
-  uint32_t qf[D / 16][4];
-#pragma unroll
-  for (int kk = 0; kk < D / 16; ++kk) {
-    qf[kk][0] = qa_ptr ? ld_u32(qa_ptr + kk * 16 + 2 * tq) : 0u;
-    qf[kk][1] = qb_ptr ? ld_u32(qb_ptr + kk * 16 + 2 * tq) : 0u;
-    qf[kk][2] = qa_ptr ? ld_u32(qa_ptr + kk * 16 + 8 + 2 * tq) : 0u;
-    qf[kk][3] = qb_ptr ? ld_u32(qb_ptr + kk * 16 + 8 + 2 * tq) : 0u;
-  }
-
-  float o[D / 8][4];
-#pragma unroll
-  for (int i = 0; i < D / 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
-  float m_a = -INFINITY, m_b = -INFINITY, l_a = 0.f, l_b = 0.f;
-
-  // the key blocks this CTA visits: cache chunks part, part+n_splits, ...; or the tree segment
-  const __nv_bfloat16* kbase;
-  const __nv_bfloat16* vbase;
-  size_t key_stride;
-  if (is_tree) {
-    kbase = k_new + (static_cast<size_t>(b) * T * Hkv + g) * D;
-    vbase = v_new + (static_cast<size_t>(b) * T * Hkv + g) * D;
-    key_stride = static_cast<size_t>(Hkv) * D;
-  } else {
-    kbase = k_cache + (static_cast<size_t>(b) * Hkv + g) * Lmax * D;
-    vbase = v_cache + (static_cast<size_t>(b) * Hkv + g) * Lmax * D;
-    key_stride = D;
-  }
-  // enumerate blocks as (start key, end key) pairs
-  auto block_range = [&](int it, int& k0, int& k1) -> bool {
-    if (is_tree) {
-      k0 = it * KB;
-      k1 = min(T, k0 + KB);
-      return k0 < T;
-    }
-    const int per_chunk = p.chunk / KB;
-    const int c = part + (it / per_chunk) * p.n_splits;
-    k0 = c * p.chunk + (it % per_chunk) * KB;
-    k1 = min(min(L, c * p.chunk + p.chunk), k0 + KB);
-    return k0 < L;
-  };
-
-  auto issue = [&](int buf, int k0, int k1) {
-    const uint32_t dk = sK + buf * KB * D * 2, dv = sV + buf * KB * D * 2;
-    for (int e = threadIdx.x; e < KB * NCH; e += blockDim.x) {
-      const int j = e / NCH, c = e % NCH;
-      const bool valid = k0 + j < k1;
-      const size_t off = static_cast<size_t>(valid ? k0 + j : k0) * key_stride + c * 8;
-      cp_async16(tile_addr<D>(dk, j, c), kbase + off, valid);
-      cp_async16(tile_addr<D>(dv, j, c), vbase + off, valid);
-    }
-    cp_async_commit();
-  };
-
-  int k0, k1;
-  bool have = block_range(0, k0, k1);
-  if (have) issue(0, k0, k1);
-  for (int it = 0; have; ++it) {
-    int n0, n1;
-    const bool have_next = block_range(it + 1, n0, n1);
-    if (have_next) issue((it + 1) & 1, n0, n1);
-    if (have_next) cp_async_wait<1>(); else cp_async_wait<0>();
-    __syncthreads();
-    const uint32_t tK = sK + (it & 1) * KB * D * 2, tV = sV + (it & 1) * KB * D * 2;
-
-    // visibility words of this block for the two rows (tree segment)
-    uint32_t wa0 = 0xffffffffu, wa1 = 0xffffffffu, wb0 = 0xffffffffu, wb1 = 0xffffffffu;
-    if (is_tree) {
-      const int w0 = k0 / 32;
-      wa0 = node_a >= 0 ? tr.mask[static_cast<size_t>(node_a) * tr.mask_words + w0] : 0u;
-      wb0 = node_b >= 0 ? tr.mask[static_cast<size_t>(node_b) * tr.mask_words + w0] : 0u;
-      wa1 = (node_a >= 0 && w0 + 1 < tr.mask_words) ? tr.mask[static_cast<size_t>(node_a) * tr.mask_words + w0 + 1] : 0u;
-      wb1 = (node_b >= 0 && w0 + 1 < tr.mask_words) ? tr.mask[static_cast<size_t>(node_b) * tr.mask_words + w0 + 1] : 0u;
-    }
-    const bool warp_active = __any_sync(0xffffffffu, (wa0 | wa1 | wb0 | wb1) != 0u) && row0 < R;
-
-    if (warp_active) {
-      float s[KB / 8][4];
-#pragma unroll
-      for (int nt = 0; nt < KB / 8; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
-#pragma unroll
-      for (int np = 0; np < KB / 16; ++np) {
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const int mat = lane >> 3, rr = lane & 7;
-          uint32_t b0, b1, b2, b3;
-          ldsm_x4(tile_addr<D>(tK, np * 16 + (mat >> 1) * 8 + rr, kk * 2 + (mat & 1)), b0, b1, b2, b3);
-          mma_bf16(s[2 * np], qf[kk], b0, b1);
-          mma_bf16(s[2 * np + 1], qf[kk], b2, b3);
-        }
-      }
-      // scale + mask, row max
-      float mx_a = -INFINITY, mx_b = -INFINITY;
-#pragma unroll
-      for (int nt = 0; nt < KB / 8; ++nt) {
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int kl = nt * 8 + 2 * tq + e;  // key offset in block
-          const bool in = k0 + kl < k1;
-          bool va = in, vb = in;
-          if (is_tree) {
-            va = in && (((kl < 32 ? wa0 >> kl : wa1 >> (kl - 32)) & 1u) != 0u);
-            vb = in && (((kl < 32 ? wb0 >> kl : wb1 >> (kl - 32)) & 1u) != 0u);
-          }
-          s[nt][e] = va ? s[nt][e] * scale_log2 : -INFINITY;
-          s[nt][2 + e] = vb ? s[nt][2 + e] * scale_log2 : -INFINITY;
-          mx_a = fmaxf(mx_a, s[nt][e]);
-          mx_b = fmaxf(mx_b, s[nt][2 + e]);
-        }
-      }
-      mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 1));
-      mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 2));
-      mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, 1));
-      mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, 2));
-      const float mn_a = fmaxf(m_a, mx_a), mn_b = fmaxf(m_b, mx_b);
-      const float al_a = mn_a == -INFINITY ? 1.f : exp2f(m_a - mn_a);
-      const float al_b = mn_b == -INFINITY ? 1.f : exp2f(m_b - mn_b);
-      m_a = mn_a;
-      m_b = mn_b;
-      float ps_a = 0.f, ps_b = 0.f;
-#pragma unroll
-      for (int nt = 0; nt < KB / 8; ++nt) {
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          s[nt][e] = mn_a == -INFINITY ? 0.f : exp2f(s[nt][e] - mn_a);
-          s[nt][2 + e] = mn_b == -INFINITY ? 0.f : exp2f(s[nt][2 + e] - mn_b);
-          ps_a += s[nt][e];
-          ps_b += s[nt][2 + e];
-        }
-      }
-      l_a = l_a * al_a + ps_a;
-      l_b = l_b * al_b + ps_b;
-#pragma unroll
-      for (int dn = 0; dn < D / 8; ++dn) {
-        o[dn][0] *= al_a;
-        o[dn][1] *= al_a;
-        o[dn][2] *= al_b;
-        o[dn][3] *= al_b;
-      }
-      // O += P V
-#pragma unroll
-      for (int kk = 0; kk < KB / 16; ++kk) {
-        uint32_t pa[4];
-        pa[0] = pack_bf16(s[2 * kk][0], s[2 * kk][1]);
-        pa[1] = pack_bf16(s[2 * kk][2], s[2 * kk][3]);
-        pa[2] = pack_bf16(s[2 * kk + 1][0], s[2 * kk + 1][1]);
-        pa[3] = pack_bf16(s[2 * kk + 1][2], s[2 * kk + 1][3]);
-#pragma unroll
-        for (int dp = 0; dp < D / 16; ++dp) {
-          const int mat = lane >> 3, rr = lane & 7;
-          uint32_t b0, b1, b2, b3;
-          ldsm_x4_t(tile_addr<D>(tV, kk * 16 + (mat & 1) * 8 + rr, dp * 2 + (mat >> 1)), b0, b1, b2, b3);
-          mma_bf16(o[2 * dp], pa, b0, b1);
-          mma_bf16(o[2 * dp + 1], pa, b2, b3);
-        }
-      }
-    }
-    __syncthreads();
-    k0 = n0;
-    k1 = n1;
-    have = have_next;
-  }
-
-  // partial results of this split
-  l_a += __shfl_xor_sync(0xffffffffu, l_a, 1);
-  l_a += __shfl_xor_sync(0xffffffffu, l_a, 2);
-  l_b += __shfl_xor_sync(0xffffffffu, l_b, 1);
-  l_b += __shfl_xor_sync(0xffffffffu, l_b, 2);
-  const size_t prow = (static_cast<size_t>(zb) * p.n_parts + part) * p.R_pad;
-  if (ra < R) {
-    float* dst = o_part + (prow + ra) * D;
-#pragma unroll
-    for (int dn = 0; dn < D / 8; ++dn)
-      *reinterpret_cast<float2*>(dst + dn * 8 + 2 * tq) = make_float2(o[dn][0], o[dn][1]);
-    if (tq == 0) ml_part[prow + ra] = make_float2(m_a, l_a);
-  }
-  if (rb < R) {
-    float* dst = o_part + (prow + rb) * D;
-#pragma unroll
-    for (int dn = 0; dn < D / 8; ++dn)
-      *reinterpret_cast<float2*>(dst + dn * 8 + 2 * tq) = make_float2(o[dn][2], o[dn][3]);
-    if (tq == 0) ml_part[prow + rb] = make_float2(m_b, l_b);
-  }
+__device__ inline bool next_seg(long long x, long long end, int& b, const AttnArgs& a, const int* s_len,
+                                const long long* s_cum, Seg& s) {
+  if (x >= end) return false;
+  while (s_cum[b + 1] <= x) ++b;
+  const int nc = cdiv(s_len[b], KB);
+  const int cost = nc + a.p.ntt;
+  const long long off = x - s_cum[b];
+  const int ui = static_cast<int>(off / cost);
+  s.b = b;
+  s.g = ui / a.p.n_qt;
+  s.qt = ui % a.p.n_qt;
+  s.nc = nc;
+  s.ustart = s_cum[b] + static_cast<long long>(ui) * cost;
+  s.uend = s.ustart + cost;
+  s.t0 = static_cast<int>(x - s.ustart);
+  s.t1 = static_cast<int>((s.uend < end ? s.uend : end) - s.ustart);
+  return true;
 }
 
-// Merge the splits: one warp per (request, node, query head).
-template <int D>
-__global__ void __launch_bounds__(256) attn_combine_kernel(int B, int T, int Hq, int Hkv, AttnPlan p,
-                                                           const float* __restrict__ o_part,
-                                                           const float2* __restrict__ ml_part, float* __restrict__ out,
-                                                           int32_t* __restrict__ dev_status) {
-  const int wid = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+// Bit j set iff some query row of query tile qt may see a key of tree tile j
+// (OR of the ancestor-mask rows of the tile's nodes).  Whole warp.
+__device__ inline uint64_t tree_tiles_visible(const AttnArgs& a, int qt) {
   const int lane = threadIdx.x & 31;
-  if (wid >= B * T * Hq) return;
-  const int hq = wid % Hq, i = (wid / Hq) % T, b = wid / (Hq * T);
-  const int g = hq / p.G, row = i * p.G + hq % p.G;
-  const size_t zrow = static_cast<size_t>(b * Hkv + g) * p.n_parts;
+  const int r0 = qt * a.p.rpt, r1 = min(a.p.R, r0 + a.p.rpt);
+  const int n0 = r0 / a.p.G, n1 = (r1 - 1) / a.p.G;
+  const int mw = a.tr.mask_words;
+  uint64_t bits = 0;
+  for (int e = lane; e < (n1 - n0 + 1) * mw; e += 32) {
+    const int node = n0 + e / mw, w = e % mw;
+    if (a.tr.mask[static_cast<size_t>(node) * mw + w]) bits |= 1ull << (w >> 1);
+  }
+  const uint32_t lo = __reduce_or_sync(0xffffffffu, static_cast<uint32_t>(bits));
+  const uint32_t hi = __reduce_or_sync(0xffffffffu, static_cast<uint32_t>(bits >> 32));
+  return (static_cast<uint64_t>(hi) << 32) | lo;
+}
+
+template <int D>
+__global__ void __launch_bounds__((kMaxWarps + 1) * 32, 1) tree_attn_kernel(
+    const __grid_constant__ CUtensorMap tm_kc, const __grid_constant__ CUtensorMap tm_vc,
+    const __grid_constant__ CUtensorMap tm_kt, const __grid_constant__ CUtensorMap tm_vt, AttnArgs a) {
+  constexpr int NSUB = D / 64;
+  constexpr uint32_t BOX = 64 * 128;
+  constexpr uint32_t HALF = NSUB * BOX;  // one K (or V) tile
+  constexpr uint32_t STAGE = 2 * HALF;
+  extern __shared__ __align__(1024) unsigned char attn_smem_raw[];
+  unsigned char* smem =
+      reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(attn_smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * STAGE);
+  uint64_t* empty = full + kStages;
+  __shared__ int s_len[MEDUSA_MAX_BATCH];
+  __shared__ long long s_cum[MEDUSA_MAX_BATCH + 1];
+
+  const AttnPlan& p = a.p;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int W = p.W;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      tc::mbar_init(full + s, 1);
+      tc::mbar_init(empty + s, W);
+    }
+    tc::fence_mbar_init();
+    tc::prefetch_tmap(&tm_kc);
+    tc::prefetch_tmap(&tm_vc);
+    tc::prefetch_tmap(&tm_kt);
+    tc::prefetch_tmap(&tm_vt);
+  }
+  pdl_wait();
+  for (int b = threadIdx.x; b < a.B; b += blockDim.x) s_len[b] = min(max(a.kv_len[b], 0), a.Lmax);
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    long long c = 0;
+    const int upb = a.Hkv * p.n_qt;
+    for (int b = 0; b < a.B; ++b) {
+      s_cum[b] = c;
+      c += static_cast<long long>(upb) * (cdiv(s_len[b], KB) + p.ntt);
+    }
+    s_cum[a.B] = c;
+  }
+  __syncthreads();
+  pdl_trigger();
+  const long long total = s_cum[a.B];
+  // the grid was sized from an upper bound of kv_len: with fewer tiles than
+  // CTAs only the first `total` CTAs take part, so that every range is non-empty
+  const long long nct = min(static_cast<long long>(gridDim.x), total);
+  if (blockIdx.x >= nct) return;
+  const long long start = blockIdx.x * total / nct, end = (blockIdx.x + 1) * total / nct;
+
+  if (warp == W) {
+    // ---------------- producer: TMA loads of K/V tiles ----------------
+    int stage = 0, issued = 0;
+    uint32_t phase = 0;
+    bool fail = false;
+    int b = 0;
+    Seg sg;
+    for (long long x = start; !fail && next_seg(x, end, b, a, s_len, s_cum, sg); x = sg.ustart + sg.t1) {
+      const uint64_t vis = tree_tiles_visible(a, sg.qt);
+      if (lane == 0) {
+        for (int t = sg.t0; t < sg.t1; ++t) {
+          const bool tree = t >= sg.nc;
+          const int j = t - sg.nc;
+          if (tree && !((vis >> j) & 1ull)) continue;
+          if (!tc::mbar_wait(empty + stage, phase ^ 1)) { fail = true; break; }
+          tc::mbar_expect_tx(full + stage, STAGE);
+          const uint32_t sk = smem_u32(smem + stage * STAGE), sv = sk + HALF;
+#pragma unroll
+          for (int h = 0; h < NSUB; ++h) {
+            if (!tree) {
+              const int z = sg.b * a.Hkv + sg.g;
+              tc::tma_load_3d(sk + h * BOX, &tm_kc, 64 * h, t * KB, z, full + stage);
+              tc::tma_load_3d(sv + h * BOX, &tm_vc, 64 * h, t * KB, z, full + stage);
+            } else {
+              const int z = sg.b * a.T + j * KB;
+              tc::tma_load_3d(sk + h * BOX, &tm_kt, 64 * h, sg.g, z, full + stage);
+              tc::tma_load_3d(sv + h * BOX, &tm_vt, 64 * h, sg.g, z, full + stage);
+            }
+          }
+          ++issued;
+          if (++stage == kStages) { stage = 0; phase ^= 1; }
+        }
+      }
+      fail = __shfl_sync(0xffffffffu, fail, 0);
+    }
+    if (lane == 0) {
+      // every issued copy must have landed before the CTA's shared memory goes away
+      for (int i = 0; i < min(issued, kStages); ++i) {
+        const int k = issued - 1 - i;
+        if (!tc::mbar_wait(full + (k % kStages), static_cast<uint32_t>((k / kStages) & 1))) fail = true;
+      }
+      if (fail && a.dev_status) atomicOr(a.dev_status, MEDUSA_DEV_TIMEOUT);
+    }
+    return;
+  }
+  if (warp > W) return;
+
+  // ---------------- consumers: 16 query rows per warp ----------------
+  const int gq = lane >> 2, tq = lane & 3;
+  const int G = p.G, R = p.R, T = a.T;
+  int stage = 0;
+  uint32_t phase = 0;
+  bool fail = false;
+  int b = 0;
+  Seg sg;
+  auto cta_of = [&](long long xx) { return static_cast<int>(((xx + 1) * nct - 1) / total); };
+  for (long long x = start; !fail && next_seg(x, end, b, a, s_len, s_cum, sg); x = sg.ustart + sg.t1) {
+    const uint64_t vis = tree_tiles_visible(a, sg.qt);
+    const int row0 = sg.qt * p.rpt + warp * 16;
+    const int ra = row0 + gq, rb = ra + 8;
+    const int node_a = ra < R ? ra / G : -1, node_b = rb < R ? rb / G : -1;
+    const __nv_bfloat16* qa = node_a >= 0 ? a.q + ((static_cast<size_t>(sg.b) * T + node_a) * a.Hq + sg.g * G + ra % G) * D : nullptr;
+    const __nv_bfloat16* qb = node_b >= 0 ? a.q + ((static_cast<size_t>(sg.b) * T + node_b) * a.Hq + sg.g * G + rb % G) * D : nullptr;
+    uint32_t qf[D / 16][4];
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+      qf[kk][0] = qa ? ld_u32(qa + kk * 16 + 2 * tq) : 0u;
+      qf[kk][1] = qb ? ld_u32(qb + kk * 16 + 2 * tq) : 0u;
+      qf[kk][2] = qa ? ld_u32(qa + kk * 16 + 8 + 2 * tq) : 0u;
+      qf[kk][3] = qb ? ld_u32(qb + kk * 16 + 8 + 2 * tq) : 0u;
+    }
+    float o[D / 8][4];
+#pragma unroll
+    for (int i = 0; i < D / 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+    float m_a = -INFINITY, m_b = -INFINITY, l_a = 0.f, l_b = 0.f;
+
+    for (int t = sg.t0; t < sg.t1; ++t) {
+      const bool tree = t >= sg.nc;
+      const int j = t - sg.nc;
+      if (tree && !((vis >> j) & 1ull)) continue;
+      if (!tc::mbar_wait(full + stage, phase)) { fail = true; break; }
+      const uint32_t tK = smem_u32(smem + stage * STAGE), tV = tK + HALF;
+      const int k0 = tree ? j * KB : t * KB;
+      const int valid = min(KB, (tree ? T : s_len[sg.b]) - k0);
+      uint32_t wa0 = 0xffffffffu, wa1 = 0xffffffffu, wb0 = 0xffffffffu, wb1 = 0xffffffffu;
+      if (tree) {
+        const int w0 = 2 * j, mw = a.tr.mask_words;
+        wa0 = node_a >= 0 ? a.tr.mask[static_cast<size_t>(node_a) * mw + w0] : 0u;
+        wb0 = node_b >= 0 ? a.tr.mask[static_cast<size_t>(node_b) * mw + w0] : 0u;
+        wa1 = (node_a >= 0 && w0 + 1 < mw) ? a.tr.mask[static_cast<size_t>(node_a) * mw + w0 + 1] : 0u;
+        wb1 = (node_b >= 0 && w0 + 1 < mw) ? a.tr.mask[static_cast<size_t>(node_b) * mw + w0 + 1] : 0u;
+      }
+      const bool active = __any_sync(0xffffffffu, (wa0 | wa1 | wb0 | wb1) != 0u) && row0 < R;
+      if (active) {
+        // the tile in two halves of 32 keys, each an online-softmax update
+#pragma unroll
+        for (int hk = 0; hk < 2; ++hk) {
+          constexpr int HK = KB / 2;
+          float s[HK / 8][4];
+#pragma unroll
+          for (int nt = 0; nt < HK / 8; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+#pragma unroll
+          for (int np = 0; np < HK / 16; ++np) {
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const int mat = lane >> 3, rr = lane & 7;
+              uint32_t b0, b1, b2, b3;
+              ldsm_x4(tile_addr(tK, hk * HK + np * 16 + (mat >> 1) * 8 + rr, kk * 2 + (mat & 1)), b0, b1, b2, b3);
+              mma_bf16(s[2 * np], qf[kk], b0, b1);
+              mma_bf16(s[2 * np + 1], qf[kk], b2, b3);
+            }
+          }
+          const uint32_t wa = hk ? wa1 : wa0, wb = hk ? wb1 : wb0;
+          float mx_a = -INFINITY, mx_b = -INFINITY;
+#pragma unroll
+          for (int nt = 0; nt < HK / 8; ++nt) {
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const int kh = nt * 8 + 2 * tq + e;  // key within the half
+              const bool in = hk * HK + kh < valid;
+              const bool va = in && ((wa >> kh) & 1u);
+              const bool vb = in && ((wb >> kh) & 1u);
+              s[nt][e] = va ? s[nt][e] * a.scale_log2 : -INFINITY;
+              s[nt][2 + e] = vb ? s[nt][2 + e] * a.scale_log2 : -INFINITY;
+              mx_a = fmaxf(mx_a, s[nt][e]);
+              mx_b = fmaxf(mx_b, s[nt][2 + e]);
+            }
+          }
+          mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 1));
+          mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 2));
+          mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, 1));
+          mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, 2));
+          const float mn_a = fmaxf(m_a, mx_a), mn_b = fmaxf(m_b, mx_b);
+          const float al_a = mn_a == -INFINITY ? 1.f : exp2f(m_a - mn_a);
+          const float al_b = mn_b == -INFINITY ? 1.f : exp2f(m_b - mn_b);
+          m_a = mn_a;
+          m_b = mn_b;
+          float ps_a = 0.f, ps_b = 0.f;
+#pragma unroll
+          for (int nt = 0; nt < HK / 8; ++nt) {
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              s[nt][e] = mn_a == -INFINITY ? 0.f : exp2f(s[nt][e] - mn_a);
+              s[nt][2 + e] = mn_b == -INFINITY ? 0.f : exp2f(s[nt][2 + e] - mn_b);
+              ps_a += s[nt][e];
+              ps_b += s[nt][2 + e];
+            }
+          }
+          l_a = l_a * al_a + ps_a;
+          l_b = l_b * al_b + ps_b;
+#pragma unroll
+          for (int dn = 0; dn < D / 8; ++dn) {
+            o[dn][0] *= al_a;
+            o[dn][1] *= al_a;
+            o[dn][2] *= al_b;
+            o[dn][3] *= al_b;
+          }
+          // O += P V.  Keys past `valid` may hold anything (cache rows beyond
+          // kv_len, another request's tree rows), so their V values are zeroed
+          // in the fragments: a zero probability times a non-finite value is NaN.
+#pragma unroll
+          for (int kk = 0; kk < HK / 16; ++kk) {
+            uint32_t pa[4];
+            pa[0] = pack_bf16(s[2 * kk][0], s[2 * kk][1]);
+            pa[1] = pack_bf16(s[2 * kk][2], s[2 * kk][3]);
+            pa[2] = pack_bf16(s[2 * kk + 1][0], s[2 * kk + 1][1]);
+            pa[3] = pack_bf16(s[2 * kk + 1][2], s[2 * kk + 1][3]);
+            const int kA = hk * HK + kk * 16 + 2 * tq, kB = kA + 8;
+            const uint32_t mA = (kA < valid ? 0x0000FFFFu : 0u) | (kA + 1 < valid ? 0xFFFF0000u : 0u);
+            const uint32_t mB = (kB < valid ? 0x0000FFFFu : 0u) | (kB + 1 < valid ? 0xFFFF0000u : 0u);
+#pragma unroll
+            for (int dp = 0; dp < D / 16; ++dp) {
+              const int mat = lane >> 3, rr = lane & 7;
+              uint32_t b0, b1, b2, b3;
+              ldsm_x4_t(tile_addr(tV, hk * HK + kk * 16 + (mat & 1) * 8 + rr, dp * 2 + (mat >> 1)), b0, b1, b2, b3);
+              mma_bf16(o[2 * dp], pa, b0 & mA, b1 & mB);
+              mma_bf16(o[2 * dp + 1], pa, b2 & mA, b3 & mB);
+            }
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(empty + stage);
+      if (++stage == kStages) { stage = 0; phase ^= 1; }
+    }
+    if (fail) break;
+
+    // ---- this segment's result: final, or a partial for the combine launch ----
+    l_a += __shfl_xor_sync(0xffffffffu, l_a, 1);
+    l_a += __shfl_xor_sync(0xffffffffu, l_a, 2);
+    l_b += __shfl_xor_sync(0xffffffffu, l_b, 1);
+    l_b += __shfl_xor_sync(0xffffffffu, l_b, 2);
+    const int c_first = cta_of(sg.ustart);
+    const int nparts = cta_of(sg.uend - 1) - c_first + 1;
+    const int hq_base = sg.g * G;
+    if (nparts == 1) {
+      if (node_a >= 0) {
+        const float inv = 1.f / l_a;
+        float* dst = a.out + ((static_cast<size_t>(sg.b) * T + node_a) * a.Hq + hq_base + ra % G) * D;
+#pragma unroll
+        for (int dn = 0; dn < D / 8; ++dn)
+          *reinterpret_cast<float2*>(dst + dn * 8 + 2 * tq) = make_float2(o[dn][0] * inv, o[dn][1] * inv);
+        if (tq == 0 && !(l_a > 0.f) && a.dev_status) atomicOr(a.dev_status + sg.b, MEDUSA_DEV_NAN);
+      }
+      if (node_b >= 0) {
+        const float inv = 1.f / l_b;
+        float* dst = a.out + ((static_cast<size_t>(sg.b) * T + node_b) * a.Hq + hq_base + rb % G) * D;
+#pragma unroll
+        for (int dn = 0; dn < D / 8; ++dn)
+          *reinterpret_cast<float2*>(dst + dn * 8 + 2 * tq) = make_float2(o[dn][2] * inv, o[dn][3] * inv);
+        if (tq == 0 && !(l_b > 0.f) && a.dev_status) atomicOr(a.dev_status + sg.b, MEDUSA_DEV_NAN);
+      }
+      continue;
+    }
+    const int slot = blockIdx.x * 2 + (start >= sg.ustart ? 0 : 1);
+    const size_t prow = static_cast<size_t>(slot) * p.rpt + warp * 16;
+    float* da = a.ws.o_part + (prow + gq) * D;
+    float* db = a.ws.o_part + (prow + gq + 8) * D;
+#pragma unroll
+    for (int dn = 0; dn < D / 8; ++dn) {
+      *reinterpret_cast<float2*>(da + dn * 8 + 2 * tq) = make_float2(o[dn][0], o[dn][1]);
+      *reinterpret_cast<float2*>(db + dn * 8 + 2 * tq) = make_float2(o[dn][2], o[dn][3]);
+    }
+    if (tq == 0) {
+      a.ws.ml_part[prow + gq] = make_float2(m_a, l_a);
+      a.ws.ml_part[prow + gq + 8] = make_float2(m_b, l_b);
+    }
+  }
+  if (fail && lane == 0 && a.dev_status) atomicOr(a.dev_status + sg.b, MEDUSA_DEV_TIMEOUT);
+}
+
+// Merge the partials of every head that spans several CTAs: one warp per
+// (head unit, query row), parts in CTA order.  The split is recomputed from
+// kv_len exactly as the attention launch made it.
+template <int D>
+__global__ void __launch_bounds__(256) attn_combine_kernel(AttnArgs a, int attn_ctas) {
+  __shared__ int s_len[MEDUSA_MAX_BATCH];
+  __shared__ long long s_cum[MEDUSA_MAX_BATCH + 1];
+  const AttnPlan& p = a.p;
+  pdl_wait();
+  for (int b = threadIdx.x; b < a.B; b += blockDim.x) s_len[b] = min(max(a.kv_len[b], 0), a.Lmax);
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    long long c = 0;
+    const int upb = a.Hkv * p.n_qt;
+    for (int b = 0; b < a.B; ++b) {
+      s_cum[b] = c;
+      c += static_cast<long long>(upb) * (cdiv(s_len[b], KB) + p.ntt);
+    }
+    s_cum[a.B] = c;
+  }
+  __syncthreads();
+  const int lane = threadIdx.x & 31;
+  const long long gw = static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (gw >= static_cast<long long>(p.units) * p.rpt) return;
+  const int unit = static_cast<int>(gw / p.rpt), row = static_cast<int>(gw % p.rpt);
+  const int qt = unit % p.n_qt, g = (unit / p.n_qt) % a.Hkv, b = unit / (p.n_qt * a.Hkv);
+  const int r = qt * p.rpt + row;
+  if (r >= p.R) return;
+  const long long total = s_cum[a.B];
+  const long long nct = min(static_cast<long long>(attn_ctas), total);
+  const int cost = cdiv(s_len[b], KB) + p.ntt;
+  const long long ustart = s_cum[b] + static_cast<long long>(g * p.n_qt + qt) * cost;
+  auto cta_of = [&](long long xx) { return static_cast<int>(((xx + 1) * nct - 1) / total); };
+  const int c_first = cta_of(ustart);
+  const int nparts = cta_of(ustart + cost - 1) - c_first + 1;
+  if (nparts == 1) return;  // written by the attention launch
+  auto part_row = [&](int q) -> size_t {
+    const int c = c_first + q;
+    const long long cs = static_cast<long long>(c) * total / nct;
+    return static_cast<size_t>(c * 2 + (cs >= ustart ? 0 : 1)) * p.rpt + row;
+  };
+  // running max and denominator over the parts (lanes take parts)
   float M = -INFINITY;
-  for (int s = 0; s < p.n_parts; ++s) {
-    const float2 ml = ml_part[(zrow + s) * p.R_pad + row];
+  for (int q = lane; q < nparts; q += 32) {
+    const float2 ml = __ldcg(a.ws.ml_part + part_row(q));
     if (ml.y > 0.f) M = fmaxf(M, ml.x);
   }
-  constexpr int PER = D / 32;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  constexpr int PER = D / 32;  // columns per lane
   float acc[PER] = {};
   float den = 0.f;
-  for (int s = 0; s < p.n_parts; ++s) {
-    const float2 ml = ml_part[(zrow + s) * p.R_pad + row];
-    if (!(ml.y > 0.f)) continue;
-    const float w = exp2f(ml.x - M);
-    den += w * ml.y;
-    const float* src = o_part + ((zrow + s) * p.R_pad + row) * D;
+  for (int q0 = 0; q0 < nparts; q0 += 32) {
+    float wq = 0.f;
+    size_t prq = 0;
+    if (q0 + lane < nparts) {
+      prq = part_row(q0 + lane);
+      const float2 ml = __ldcg(a.ws.ml_part + prq);
+      if (ml.y > 0.f) {
+        wq = exp2f(ml.x - M);
+        den = fmaf(wq, ml.y, den);
+      }
+    }
+    const int nq = min(32, nparts - q0);
+    constexpr int UQ = 8;
+    for (int j0 = 0; j0 < nq; j0 += UQ) {
+      float v[UQ][PER];
+      float wj[UQ];
 #pragma unroll
-    for (int e = 0; e < PER; ++e) acc[e] += w * src[lane + 32 * e];
+      for (int j = 0; j < UQ; ++j) {
+        wj[j] = __shfl_sync(0xffffffffu, wq, (j0 + j) & 31);
+        const size_t pr = __shfl_sync(0xffffffffu, prq, (j0 + j) & 31);
+        if (j0 + j < nq) {
+          const float* src = a.ws.o_part + pr * D + lane * PER;
+          if constexpr (PER == 4) {
+            const float4 t = __ldcg(reinterpret_cast<const float4*>(src));
+            v[j][0] = t.x; v[j][1] = t.y; v[j][2] = t.z; v[j][3] = t.w;
+          } else {
+            const float2 t = __ldcg(reinterpret_cast<const float2*>(src));
+            v[j][0] = t.x; v[j][1] = t.y;
+          }
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < UQ; ++j)
+        if (j0 + j < nq)
+#pragma unroll
+          for (int e = 0; e < PER; ++e) acc[e] = fmaf(wj[j], v[j][e], acc[e]);
+    }
   }
-  float* dst = out + ((static_cast<size_t>(b) * T + i) * Hq + hq) * D;
-  const float inv = 1.f / den;
 #pragma unroll
-  for (int e = 0; e < PER; ++e) dst[lane + 32 * e] = acc[e] * inv;
-  if (lane == 0 && !(den > 0.f) && dev_status) atomicOr(dev_status + b, MEDUSA_DEV_NAN);
+  for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+  const int node = r / p.G;
+  float* dst = a.out + ((static_cast<size_t>(b) * a.T + node) * a.Hq + g * p.G + r % p.G) * D + lane * PER;
+  const float inv = 1.f / den;
+  if constexpr (PER == 4) {
+    *reinterpret_cast<float4*>(dst) = make_float4(acc[0] * inv, acc[1] * inv, acc[2] * inv, acc[3] * inv);
+  } else {
+    *reinterpret_cast<float2*>(dst) = make_float2(acc[0] * inv, acc[1] * inv);
+  }
+  if (lane == 0 && !(den > 0.f) && a.dev_status) atomicOr(a.dev_status + b, MEDUSA_DEV_NAN);
 }
 
 // Exact fp32 path: one CTA per (request, node, query head); scores in smem.
@@ -343,6 +569,7 @@ __global__ void __launch_bounds__(128) tree_attn_f32_kernel(medusa_tree_dev tr, 
                                                             int D, int Lmax, float scale, float* __restrict__ out) {
   extern __shared__ float sc[];  // [Lmax + T]
   __shared__ float red[32];
+  pdl_wait();
   const int hq = blockIdx.x % Hq, i = (blockIdx.x / Hq) % tr.T, b = blockIdx.x / (Hq * tr.T);
   const int T = tr.T;
   const int g = hq / (Hq / Hkv);
@@ -404,9 +631,60 @@ MEDUSA_API size_t medusa_tree_attention_workspace_size(const medusa_tree* tree, 
                                                        medusa_dtype dtype) {
   if (!tree || B < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv || Lmax < 0) return 0;
   if (dtype == MEDUSA_F32) return 256;
-  AttnPlan p = plan_attn(tree->T, B, Hq, Hkv, Lmax, kv_len_hint);
-  return attn_ws_bytes(p, B, Hkv, D);
+  AttnPlan p = plan_attn(tree->T, B, Hq, Hkv, Lmax, kv_len_hint, sm_count());
+  return carve_attn_ws(nullptr, p, D).bytes;
 }
+
+namespace {
+
+template <int D>
+int launch_attn_bf16(const medusa_tree* tree, const void* q, const void* k_new, const void* v_new,
+                     const void* k_cache, const void* v_cache, const int32_t* kv_len, int B, int Hq, int Hkv,
+                     int Lmax, float scale, float* out, const AttnPlan& p, const AttnWs& w, int32_t* dev_status,
+                     cudaStream_t st) {
+  const int T = tree->T;
+  CUtensorMap kc, vc, kt, vt;
+  const uint64_t rowb = static_cast<uint64_t>(D) * 2;
+  const uint64_t lm = static_cast<uint64_t>(std::max(Lmax, 1));
+  if (!make_tmap_bf16_3d(&kc, k_cache, D, lm, static_cast<uint64_t>(B) * Hkv, rowb, lm * rowb, KB, 1) ||
+      !make_tmap_bf16_3d(&vc, v_cache, D, lm, static_cast<uint64_t>(B) * Hkv, rowb, lm * rowb, KB, 1) ||
+      !make_tmap_bf16_3d(&kt, k_new, D, Hkv, static_cast<uint64_t>(B) * T, rowb, Hkv * rowb, 1, KB) ||
+      !make_tmap_bf16_3d(&vt, v_new, D, Hkv, static_cast<uint64_t>(B) * T, rowb, Hkv * rowb, 1, KB))
+    return MEDUSA_ERR_CUDA;
+  AttnArgs a{};
+  a.tr = tree->dev;
+  a.q = static_cast<const __nv_bfloat16*>(q);
+  a.kv_len = kv_len;
+  a.out = out;
+  a.ws = w;
+  a.dev_status = dev_status;
+  a.B = B;
+  a.T = T;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.Lmax = Lmax;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.p = p;
+  const size_t smem = 1024 + static_cast<size_t>(kStages) * 2 * (D / 64) * 8192 + 2 * kStages * 8;
+  auto k = tree_attn_kernel<D>;
+  if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) != cudaSuccess)
+    return MEDUSA_ERR_CUDA;
+  if (launch_pdl(k, dim3(p.nctas), dim3((p.W + 1) * 32), smem, st, kc, vc, kt, vt, a) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return MEDUSA_ERR_CUDA;
+  }
+  MEDUSA_LAUNCH_CHECK();
+  const long long warps = static_cast<long long>(p.units) * p.rpt;
+  if (launch_pdl(attn_combine_kernel<D>, dim3(static_cast<unsigned>((warps + 7) / 8)), dim3(256), 0, st, a,
+                 p.nctas) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return MEDUSA_ERR_CUDA;
+  }
+  MEDUSA_LAUNCH_CHECK();
+  return MEDUSA_OK;
+}
+
+}  // namespace
 
 MEDUSA_API int medusa_tree_attention(const medusa_tree* tree, const void* q, const void* k_new, const void* v_new,
                                      const void* k_cache, const void* v_cache, const int32_t* kv_len, int32_t B,
@@ -429,44 +707,22 @@ MEDUSA_API int medusa_tree_attention(const medusa_tree* tree, const void* q, con
     if (cudaFuncSetAttribute(tree_attn_f32_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem)) != cudaSuccess)
       return MEDUSA_ERR_CUDA;
-    tree_attn_f32_kernel<<<B * T * Hq, 128, smem, st>>>(
-        tree->dev, static_cast<const float*>(q), static_cast<const float*>(k_new), static_cast<const float*>(v_new),
-        static_cast<const float*>(k_cache), static_cast<const float*>(v_cache), kv_len, Hq, Hkv, D, Lmax, scale, out);
+    if (launch_pdl(tree_attn_f32_kernel, dim3(B * T * Hq), dim3(128), smem, st, tree->dev,
+                   static_cast<const float*>(q), static_cast<const float*>(k_new), static_cast<const float*>(v_new),
+                   static_cast<const float*>(k_cache), static_cast<const float*>(v_cache), kv_len, Hq, Hkv, D, Lmax,
+                   scale, out) != cudaSuccess) {
+      (void)cudaGetLastError();
+      return MEDUSA_ERR_CUDA;
+    }
     MEDUSA_LAUNCH_CHECK();
     return MEDUSA_OK;
   }
-  AttnPlan p = plan_attn(T, B, Hq, Hkv, Lmax, kv_len_hint);
-  const size_t need = attn_ws_bytes(p, B, Hkv, D);
-  if (!ws || ws_bytes < need) return MEDUSA_ERR_WORKSPACE;
-  const size_t nrow = static_cast<size_t>(B) * Hkv * p.n_parts * p.R_pad;
-  float* o_part = static_cast<float*>(ws);
-  float2* ml_part = reinterpret_cast<float2*>(static_cast<char*>(ws) + align_up(nrow * D * 4, 256));
-  const size_t smem = 4 * static_cast<size_t>(KB) * D * 2;
-  dim3 grid(p.n_parts, p.n_qt, B * Hkv);
-  const float scale_log2 = scale * 1.4426950408889634f;
-  const int cthreads = 256;
-  const int cblocks = cdiv(B * T * Hq, cthreads / 32);
-  if (D == 128) {
-    if (cudaFuncSetAttribute(tree_attn_bf16_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem)) != cudaSuccess)
-      return MEDUSA_ERR_CUDA;
-    tree_attn_bf16_kernel<128><<<grid, p.nwarps * 32, smem, st>>>(
-        tree->dev, static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k_new),
-        static_cast<const __nv_bfloat16*>(v_new), static_cast<const __nv_bfloat16*>(k_cache),
-        static_cast<const __nv_bfloat16*>(v_cache), kv_len, Hq, Hkv, Lmax, p, scale_log2, o_part, ml_part);
-    MEDUSA_LAUNCH_CHECK();
-    attn_combine_kernel<128><<<cblocks, cthreads, 0, st>>>(B, T, Hq, Hkv, p, o_part, ml_part, out, dev_status);
-  } else {
-    if (cudaFuncSetAttribute(tree_attn_bf16_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem)) != cudaSuccess)
-      return MEDUSA_ERR_CUDA;
-    tree_attn_bf16_kernel<64><<<grid, p.nwarps * 32, smem, st>>>(
-        tree->dev, static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k_new),
-        static_cast<const __nv_bfloat16*>(v_new), static_cast<const __nv_bfloat16*>(k_cache),
-        static_cast<const __nv_bfloat16*>(v_cache), kv_len, Hq, Hkv, Lmax, p, scale_log2, o_part, ml_part);
-    MEDUSA_LAUNCH_CHECK();
-    attn_combine_kernel<64><<<cblocks, cthreads, 0, st>>>(B, T, Hq, Hkv, p, o_part, ml_part, out, dev_status);
-  }
-  MEDUSA_LAUNCH_CHECK();
-  return MEDUSA_OK;
+  AttnPlan p = plan_attn(T, B, Hq, Hkv, Lmax, kv_len_hint, sm_count());
+  AttnWs w = carve_attn_ws(ws, p, D);
+  if (!ws || ws_bytes < w.bytes) return MEDUSA_ERR_WORKSPACE;
+  if (D == 128)
+    return launch_attn_bf16<128>(tree, q, k_new, v_new, k_cache, v_cache, kv_len, B, Hq, Hkv, Lmax, scale, out, p, w,
+                                 dev_status, st);
+  return launch_attn_bf16<64>(tree, q, k_new, v_new, k_cache, v_cache, kv_len, B, Hq, Hkv, Lmax, scale, out, p, w,
+                              dev_status, st);
 }

@@ -94,11 +94,37 @@ __device__ inline uint64_t globaltimer_ns() {
   return t;
 }
 
+// Programmatic dependent launch: wait until the grids this one depends on have
+// completed and their writes are visible (a no-op when launched without the
+// attribute), and let the next grid in the stream start launching.
+__device__ inline void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ inline void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // Bounded-wait limit for every device-side spin (about one second).
 constexpr uint64_t kSpinLimitNs = 1000000000ull;
 
 // Process-wide count of kernels this library has launched (or captured).
 void note_launch();
+
+// Launch `kernel` with programmatic dependent launch allowed: the grid may
+// start while the previous kernel in the stream is still finishing, and the
+// kernel itself waits (pdl_wait) before it touches what that work produced.
+// Every kernel launched this way calls pdl_wait in all of its CTAs.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
 
 }  // namespace medusa
 

@@ -22,37 +22,89 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
-constexpr int kRows = 4;  // weight rows per warp pass
-constexpr int kTargetCtas = 148 * 4;
+constexpr int kRows = 4;  // most weight rows per warp pass
 constexpr size_t kMaxXBytes = 96 * 1024;  // activation rows staged per launch
 
-template <int BMAX> struct Unroll { static constexpr int U = BMAX <= 2 ? 4 : 2; };
+// Rows per warp pass (R) and 16-byte chunks per lane and row in flight (U):
+// R*U = 16 loads in flight per lane.  With one or two activation rows a pass
+// is one whole weight row (H = 4096 bf16 is 512 chunks = 16 per lane), so the
+// warps' shares differ by at most one row; with more activation rows several
+// weight rows share each staged activation chunk.
+template <int BMAX> struct Pass {
+  static constexpr int R = BMAX <= 2 ? 1 : BMAX <= 4 ? 2 : 4;
+  static constexpr int U = BMAX <= 2 ? 16 : BMAX <= 4 ? 4 : 2;
+};
 
+// Work split.  Both launches size their grid to the CTAs that are resident at
+// once (one wave) and split the weight rows evenly: first across CTAs, then
+// across the warps of a CTA, so no SM or warp carries a whole extra row group
+// at the end.  K2 gives every head (block) the same number of CTAs, so each
+// CTA's rows lie inside one head and its top-k candidates belong to that head.
 struct HeadsPlan {
   int nblk;     // K heads (+1 for the lm_head root block)
-  int groups;   // row groups of kRows per warp
-  int rpc;      // rows per CTA
   int cph;      // CTAs per block (head)
+  int rpc;      // most rows one K2 CTA holds
   int bgroup;   // batch rows per launch
-  int fc_groups;
   int fc_ctas;
 };
 
-HeadsPlan plan_heads(int B, int H, int V, int K, int with_root, int esize) {
+int device_sms() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return 148;
+  }
+  return n;
+}
+
+constexpr size_t kSmemTwoPerSm = 110 * 1024;   // two CTAs per SM fit below this
+constexpr size_t kSmemMax = 220 * 1024;        // per-CTA dynamic shared memory used at most
+
+// K2 shared memory: staged activations, then one region holding first the
+// CTA's logits [bmax][rpc] and, in the CTA that merges a head, every CTA's
+// candidates [cph][topk] (values and ids), then per-warp and final top-k.
+__host__ __device__ inline size_t vocab_region_floats(int bmax, int rpc, int cph, int topk) {
+  const size_t z = static_cast<size_t>(bmax) * rpc, m = 2 * static_cast<size_t>(cph) * topk;
+  return z > m ? z : m;
+}
+size_t vocab_smem_bytes(int nb, int bmax, int H, int esize, int rpc, int cph, int topk) {
+  return align_up(static_cast<size_t>(nb) * H * esize, 16) +
+         (vocab_region_floats(bmax, rpc, cph, topk) + 2 * kWarps * static_cast<size_t>(topk) +
+          2 * static_cast<size_t>(topk)) * 4;
+}
+
+int bmax_of(int nb) { return nb == 1 ? 1 : nb == 2 ? 2 : nb <= 4 ? 4 : nb <= 8 ? 8 : 16; }
+
+// Returns false when no split fits in shared memory.
+bool plan_heads(int B, int H, int V, int K, int with_root, int esize, int topk, HeadsPlan* out) {
   HeadsPlan p{};
+  const int sms = device_sms();
   p.nblk = K + (with_root ? 1 : 0);
-  const long rows = static_cast<long>(p.nblk) * V;
-  p.groups = std::max(1L, (rows + static_cast<long>(kTargetCtas) * kWarps * kRows - 1) /
-                              (static_cast<long>(kTargetCtas) * kWarps * kRows));
-  p.rpc = p.groups * kWarps * kRows;
-  p.cph = cdiv(V, p.rpc);
   p.bgroup = static_cast<int>(std::min<size_t>(16, std::max<size_t>(1, kMaxXBytes / (static_cast<size_t>(H) * esize))));
   p.bgroup = std::min(p.bgroup, B);
+  const int bm = bmax_of(p.bgroup);
+  auto smem_of = [&](int cph) { return vocab_smem_bytes(p.bgroup, bm, H, esize, cdiv(V, cph), cph, topk); };
+  // K2: one wave at two CTAs per SM (the GEMV is register-bound there), else one
+  // wave at one CTA per SM, else as many CTAs as the per-CTA logit buffer needs
+  int cph = std::max(1, std::min(2 * sms / p.nblk, V));
+  if (smem_of(cph) > kSmemTwoPerSm) {
+    cph = std::max(1, std::min(sms / p.nblk, V));
+    const long fixed = static_cast<long>(align_up(static_cast<size_t>(p.bgroup) * H * esize, 16)) +
+                       (2L * kWarps * topk + 2L * topk) * 4;
+    const long budget = static_cast<long>(kSmemMax) - fixed;  // bytes for the logit/candidate region
+    if (budget < 4L * bm) return false;
+    const long rows_fit = budget / (4L * bm);
+    cph = std::max<long>(cph, (V + rows_fit - 1) / rows_fit);
+    cph = std::min(cph, V);
+    if (smem_of(cph) > kSmemMax) return false;
+  }
+  p.cph = cph;
+  p.rpc = cdiv(V, p.cph);
   const long fc_rows = static_cast<long>(K) * H;
-  p.fc_groups = std::max(1L, (fc_rows + static_cast<long>(kTargetCtas) * kWarps * kRows - 1) /
-                                 (static_cast<long>(kTargetCtas) * kWarps * kRows));
-  p.fc_ctas = static_cast<int>(cdiv(static_cast<int>(fc_rows), p.fc_groups * kWarps * kRows));
-  return p;
+  const int fc_occ = static_cast<size_t>(p.bgroup) * H * esize > kSmemTwoPerSm ? 1 : 2;
+  p.fc_ctas = static_cast<int>(std::max(1L, std::min(static_cast<long>(sms) * fc_occ, fc_rows)));
+  *out = p;
+  return true;
 }
 
 struct HeadsWs {
@@ -79,25 +131,42 @@ HeadsWs carve_heads_ws(void* base, const HeadsPlan& p, int B, int H, int K, int 
   return w;
 }
 
-// K1: one warp pass = kRows rows of W1 (flattened [K*H] rows) against nb rows of h.
+// Ask L2 for the first 4 KB of up to kRows weight rows (one 128-byte line per
+// lane and row).  Weights are constant inputs of the step, so this may run
+// before the wait on the preceding kernel.
+template <typename T>
+__device__ inline void prefetch_rows(const T* W, long row0, long rows, int H) {
+  const int lane = threadIdx.x & 31;
+  const long row_bytes = static_cast<long>(H) * sizeof(T);
+  if (lane * 128L >= row_bytes) return;
+  for (long r = row0; r < row0 + kRows && r < row0 + rows; ++r)
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<const char*>(W + r * H) + lane * 128));
+}
+
+// K1: rows [c*N/C, (c+1)*N/C) of W1 (flattened [K*H] rows) for CTA c, split
+// evenly over its warps; each warp dots Pass::R rows at a time with nb rows of h.
 template <typename T, int BMAX>
 __global__ void __launch_bounds__(kThreads) heads_fc_kernel(const T* __restrict__ h, const T* __restrict__ W1,
                                                             const T* __restrict__ b1, int H, int K, int nb,
-                                                            int groups, T* __restrict__ u) {
+                                                            T* __restrict__ u) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   T* xs = reinterpret_cast<T*>(smem_raw);
-  stage_rows(xs, h, H, nb, H);
-  __syncthreads();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const long nrows = static_cast<long>(K) * H;
-  for (int g = 0; g < groups; ++g) {
-    const long row0 = (static_cast<long>(blockIdx.x) * groups * kWarps + static_cast<long>(g) * kWarps + warp) * kRows;
-    if (row0 >= nrows) break;
-    const int valid = nrows - row0 < kRows ? static_cast<int>(nrows - row0) : kRows;
-    float acc[kRows][BMAX];
-    gemv_rows<T, BMAX, kRows, Unroll<BMAX>::U>(W1, row0, valid, H, xs, nb, acc);
+  const long c0 = blockIdx.x * nrows / gridDim.x, c1 = (blockIdx.x + 1) * nrows / gridDim.x;
+  const long w0 = c0 + warp * (c1 - c0) / kWarps, w1 = c0 + (warp + 1) * (c1 - c0) / kWarps;
+  prefetch_rows(W1, w0, w1 - w0, H);
+  pdl_wait();
+  pdl_trigger();
+  stage_rows(xs, h, H, nb, H);
+  __syncthreads();
+  constexpr int R = Pass<BMAX>::R;
+  for (long row0 = w0; row0 < w1; row0 += R) {
+    const int valid = w1 - row0 < R ? static_cast<int>(w1 - row0) : R;
+    float acc[R][BMAX];
+    gemv_rows<T, BMAX, R, Pass<BMAX>::U>(W1, row0, valid, H, xs, nb, acc);
 #pragma unroll
-    for (int r = 0; r < kRows; ++r) {
+    for (int r = 0; r < R; ++r) {
 #pragma unroll
       for (int b = 0; b < BMAX; ++b) {
         if (r < valid && b < nb && lane == ((r * BMAX + b) & 31)) {
@@ -113,12 +182,13 @@ __global__ void __launch_bounds__(kThreads) heads_fc_kernel(const T* __restrict_
   }
 }
 
-// K2: CTA = slice [v0, v0+rpc) of one block's vocabulary rows.  Block j < K is
-// head j (weights W2_j, activations u[:, j]); block K is lm_head on h (root).
+// K2: CTA j of block blk holds rows [j*V/cph, (j+1)*V/cph) of that block.
+// Block blk < K is head blk (weights W2_blk, activations u[:, blk]); block K is
+// lm_head on h (root).
 template <typename T, int BMAX>
 __global__ void __launch_bounds__(kThreads) heads_vocab_kernel(
     const T* __restrict__ h, const T* __restrict__ u, const T* __restrict__ W2, const T* __restrict__ lm_head,
-    int B, int b0, int nb, int H, int V, int K, int topk, int groups, int rpc, int cph,
+    int B, int b0, int nb, int H, int V, int K, int topk, int rpc, int cph,
     float* __restrict__ head_logits, int32_t* __restrict__ topk_ids, float* __restrict__ topk_vals,
     int32_t* __restrict__ root_tok, float* __restrict__ cand_v, int* __restrict__ cand_i, int* __restrict__ counters) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
@@ -131,34 +201,38 @@ __global__ void __launch_bounds__(kThreads) heads_vocab_kernel(
 
   T* xs = reinterpret_cast<T*>(smem_raw);
   float* zs = reinterpret_cast<float*>(smem_raw + align_up(static_cast<size_t>(nb) * H * sizeof(T), 16));
-  float* mv = zs + static_cast<size_t>(BMAX) * rpc;          // merge buffer values [cph * topk]
+  // the merge buffers reuse the logit region once the local top-k is out
+  float* mv = zs;                                             // [cph * topk]
   int* mi = reinterpret_cast<int*>(mv + static_cast<size_t>(cph) * topk);
-  float* sv = reinterpret_cast<float*>(mi + static_cast<size_t>(cph) * topk);  // [kWarps * topk]
+  float* sv = zs + vocab_region_floats(BMAX, rpc, cph, topk);  // [kWarps * topk]
   int* si = reinterpret_cast<int*>(sv + kWarps * topk);
   float* fv = reinterpret_cast<float*>(si + kWarps * topk);  // [topk] final
   int* fi = reinterpret_cast<int*>(fv + topk);
   __shared__ int s_last;
 
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int v0 = static_cast<int>(static_cast<long>(cta) * V / cph);
+  const int n = static_cast<int>(static_cast<long>(cta + 1) * V / cph) - v0;
+  const int lr0 = warp * n / kWarps, lr1 = (warp + 1) * n / kWarps;  // this warp's local rows
+  prefetch_rows(W, v0 + lr0, lr1 - lr0, H);
+  pdl_wait();
+  pdl_trigger();
   stage_rows(xs, x, x_stride, nb, H);
   __syncthreads();
 
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int v0 = cta * rpc;
-  const int n = min(rpc, V - v0);
-  for (int g = 0; g < groups; ++g) {
-    const int lr0 = (g * kWarps + warp) * kRows;
-    if (lr0 >= n) break;
-    const int valid = min(kRows, n - lr0);
-    float acc[kRows][BMAX];
-    gemv_rows<T, BMAX, kRows, Unroll<BMAX>::U>(W, static_cast<size_t>(v0 + lr0), valid, H, xs, nb, acc);
+  constexpr int R = Pass<BMAX>::R;
+  for (int lr = lr0; lr < lr1; lr += R) {
+    const int valid = min(R, lr1 - lr);
+    float acc[R][BMAX];
+    gemv_rows<T, BMAX, R, Pass<BMAX>::U>(W, static_cast<size_t>(v0 + lr), valid, H, xs, nb, acc);
 #pragma unroll
-    for (int r = 0; r < kRows; ++r) {
+    for (int r = 0; r < R; ++r) {
 #pragma unroll
       for (int b = 0; b < BMAX; ++b) {
         if (r < valid && b < nb && lane == ((r * BMAX + b) & 31)) {
-          zs[static_cast<size_t>(b) * rpc + lr0 + r] = acc[r][b];
+          zs[static_cast<size_t>(b) * rpc + lr + r] = acc[r][b];
           if (head_logits && !is_root)
-            head_logits[(static_cast<size_t>(b0 + b) * K + blk) * V + v0 + lr0 + r] = acc[r][b];
+            head_logits[(static_cast<size_t>(b0 + b) * K + blk) * V + v0 + lr + r] = acc[r][b];
         }
       }
     }
@@ -169,8 +243,8 @@ __global__ void __launch_bounds__(kThreads) heads_vocab_kernel(
   for (int b = 0; b < nb; ++b) {
     float* outv = cand_v + ((static_cast<size_t>(blk) * B + b0 + b) * cph + cta) * topk;
     int* outi = cand_i + ((static_cast<size_t>(blk) * B + b0 + b) * cph + cta) * topk;
-    block_topk(zs + static_cast<size_t>(b) * rpc, nullptr, v0, n, kk, mv, mi, sv, si);
-    for (int t = threadIdx.x; t < kk; t += blockDim.x) { outv[t] = mv[t]; outi[t] = mi[t]; }
+    block_topk(zs + static_cast<size_t>(b) * rpc, nullptr, v0, n, kk, fv, fi, sv, si);
+    for (int t = threadIdx.x; t < kk; t += blockDim.x) { outv[t] = fv[t]; outi[t] = fi[t]; }
     __syncthreads();
   }
 
@@ -212,17 +286,22 @@ int launch_heads(const HeadsPlan& p, const HeadsWs& w, const T* h, const T* W1, 
   auto fc = heads_fc_kernel<T, BMAX>;
   if (cudaFuncSetAttribute(fc, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(xbytes)) != cudaSuccess)
     return MEDUSA_ERR_CUDA;
-  fc<<<p.fc_ctas, kThreads, xbytes, st>>>(h + static_cast<size_t>(b0) * H, W1, b1, H, K, nb, p.fc_groups,
-                                          static_cast<T*>(w.u) + static_cast<size_t>(b0) * K * H);
+  if (launch_pdl(fc, dim3(p.fc_ctas), dim3(kThreads), xbytes, st, h + static_cast<size_t>(b0) * H, W1, b1, H, K, nb,
+                 static_cast<T*>(w.u) + static_cast<size_t>(b0) * K * H) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return MEDUSA_ERR_CUDA;
+  }
   MEDUSA_LAUNCH_CHECK();
-  const size_t smem = xbytes + (static_cast<size_t>(BMAX) * p.rpc + 2 * static_cast<size_t>(p.cph) * topk +
-                                2 * kWarps * static_cast<size_t>(topk) + 2 * static_cast<size_t>(topk)) * 4;
+  const size_t smem = vocab_smem_bytes(nb, BMAX, H, sizeof(T), p.rpc, p.cph, topk);
   auto vk = heads_vocab_kernel<T, BMAX>;
   if (cudaFuncSetAttribute(vk, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) != cudaSuccess)
     return MEDUSA_ERR_CUDA;
-  vk<<<p.nblk * p.cph, kThreads, smem, st>>>(h, static_cast<const T*>(w.u), W2, lm, B, b0, nb, H, V, K, topk,
-                                             p.groups, p.rpc, p.cph, head_logits, topk_ids, topk_vals, root_tok,
-                                             w.cand_v, w.cand_i, w.counters);
+  if (launch_pdl(vk, dim3(p.nblk * p.cph), dim3(kThreads), smem, st, h, static_cast<const T*>(w.u), W2, lm, B, b0, nb,
+                 H, V, K, topk, p.rpc, p.cph, head_logits, topk_ids, topk_vals, root_tok, w.cand_v, w.cand_i,
+                 w.counters) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return MEDUSA_ERR_CUDA;
+  }
   MEDUSA_LAUNCH_CHECK();
   return MEDUSA_OK;
 }
@@ -250,7 +329,8 @@ MEDUSA_API size_t medusa_heads_topk_workspace_size(int32_t B, int32_t H, int32_t
                                                    int32_t with_lm_head, medusa_dtype dtype) {
   if (B < 1 || H < 8 || V < 1 || K < 1 || topk < 1) return 0;
   const int es = dtype == MEDUSA_BF16 ? 2 : 4;
-  HeadsPlan p = plan_heads(B, H, V, K, with_lm_head, es);
+  HeadsPlan p;
+  if (!plan_heads(B, H, V, K, with_lm_head, es, topk, &p)) return 0;
   return carve_heads_ws(nullptr, p, B, H, K, topk, es).bytes;
 }
 
@@ -268,7 +348,8 @@ MEDUSA_API int medusa_heads_topk(const void* h, const void* w1, const void* b1, 
     if (q && !aligned16(q)) return MEDUSA_ERR_ALIGNMENT;
   if ((lm_head && !aligned16(lm_head)) || (head_logits && !aligned16(head_logits))) return MEDUSA_ERR_ALIGNMENT;
   const int es = dtype == MEDUSA_BF16 ? 2 : 4;
-  HeadsPlan p = plan_heads(B, H, V, K, lm_head != nullptr, es);
+  HeadsPlan p;
+  if (!plan_heads(B, H, V, K, lm_head != nullptr, es, topk, &p)) return MEDUSA_ERR_UNSUPPORTED;
   HeadsWs w = carve_heads_ws(ws, p, B, H, K, topk, es);
   if (!ws || ws_bytes < w.bytes) return MEDUSA_ERR_WORKSPACE;
   auto st = reinterpret_cast<cudaStream_t>(stream);
@@ -334,7 +415,8 @@ MEDUSA_API int medusa_heads_topk_noalloc(const void* h, const void* w1, const vo
     if (!aligned16(q)) return MEDUSA_ERR_ALIGNMENT;
   if ((lm_head && !aligned16(lm_head)) || (head_logits && !aligned16(head_logits))) return MEDUSA_ERR_ALIGNMENT;
   const int es = dtype == MEDUSA_BF16 ? 2 : 4;
-  HeadsPlan p = plan_heads(B, H, V, K, lm_head != nullptr, es);
+  HeadsPlan p;
+  if (!plan_heads(B, H, V, K, lm_head != nullptr, es, topk, &p)) return MEDUSA_ERR_UNSUPPORTED;
   if (carve_heads_ws(nullptr, p, B, H, K, topk, es).bytes > kNoAllocScratchBytes) return MEDUSA_ERR_SCRATCH_LIMIT;
   void* scratch = nullptr;
   const int rc = heads_scratch_address(&scratch);

@@ -44,6 +44,18 @@ __device__ inline void prefetch_tmap(const CUtensorMap* m) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
 }
 
+// 3-D tiled TMA load completing on `bar`.
+__device__ inline void tma_load_3d(uint32_t dst, const CUtensorMap* m, int x, int y, int z, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];"
+      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ inline void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
 // 2-D tiled TMA load (x = innermost element coordinate, y = row) completing on `bar`.
 __device__ inline void tma_load_2d(uint32_t dst, const CUtensorMap* m, int x, int y, uint64_t* bar) {
   asm volatile(
@@ -124,5 +136,10 @@ EncodeTiledFn encode_tiled_fn();
 
 // 2-D bf16 row-major [rows, cols] map with a {64, box_rows} box and 128-byte swizzle.
 bool make_tmap_bf16(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows);
+
+// 3-D bf16 map: dims {d0 (innermost, elements), d1, d2}, byte strides of d1 and d2,
+// box {64, box1, box2}, 128-byte swizzle; out-of-range elements read as zero.
+bool make_tmap_bf16_3d(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
+                       uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t box1, uint32_t box2);
 
 }  // namespace medusa

@@ -169,6 +169,7 @@ __global__ void build_tree_kernel(medusa_tree_dev tr, const int32_t* __restrict_
                                   int32_t* __restrict__ dev_status) {
   const int b = blockIdx.x;
   const int T = tr.T;
+  pdl_wait();
   const int32_t L = kv_len[b];
   const int32_t root = root_tok[b];
   bool bad = root < 0;
@@ -205,8 +206,11 @@ MEDUSA_API int medusa_build_tree(const medusa_tree* tree, const int32_t* root_to
   if (!aligned16(root_tok) || !aligned16(topk_ids) || !aligned16(kv_len) || !aligned16(tree_tokens) ||
       !aligned16(position_ids) || (candidates && !aligned16(candidates)) || (dev_status && !aligned16(dev_status)))
     return MEDUSA_ERR_ALIGNMENT;
-  build_tree_kernel<<<B, 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
-      tree->dev, root_tok, topk_ids, K, topk, kv_len, tree_tokens, position_ids, candidates, dev_status);
+  if (launch_pdl(build_tree_kernel, dim3(B), dim3(256), 0, reinterpret_cast<cudaStream_t>(stream), tree->dev,
+                 root_tok, topk_ids, K, topk, kv_len, tree_tokens, position_ids, candidates, dev_status) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return MEDUSA_ERR_CUDA;
+  }
   MEDUSA_LAUNCH_CHECK();
   return MEDUSA_OK;
 }

@@ -57,13 +57,25 @@ bool make_tmap_bf16(CUtensorMap* m, const void* base, uint64_t rows, uint64_t co
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool make_tmap_bf16_3d(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
+                       uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t box1, uint32_t box2) {
+  EncodeTiledFn enc = encode_tiled_fn();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {d0, d1, d2};
+  cuuint64_t strides[2] = {stride1_bytes, stride2_bytes};
+  cuuint32_t box[3] = {64, box1, box2};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace medusa
 
 namespace {
 
 constexpr int BM = 128;
 constexpr int BK = 64;
-constexpr int STAGES = 4;
 constexpr int F32_TILE = 256;  // vocabulary columns per statistics tile on the fp32 path
 
 struct VerifyPlan {
@@ -127,22 +139,37 @@ struct EpiArgs {
 
 // ------------------------------------------------------------------------
 // K5, bf16: tcgen05 GEMM with the statistics epilogue.
-// 192 threads: warps 0-3 epilogue (TMEM lanes 0-127), warp 4 TMA producer,
-// warp 5 MMA issuer and TMEM owner.
+// 224 threads: warps 0-3 epilogue (TMEM lanes 0-127), warp 4 streams lm_head
+// tiles, warp 5 issues the MMAs and owns TMEM, warp 6 streams the tree rows X.
+// lm_head (from HBM) and X (from L2, shared by every CTA) run in separate
+// rings: a deep one for the weight stream, a shallow one for X, whose stage
+// holds only the xr rows the tile has (xr <= 128; the MMA's reads of rows
+// xr..127 land in the next stage's bytes and only feed accumulator rows that
+// are never read).  Each CTA starts its k loop at its own offset so the CTAs
+// do not all read the same block of X at the same moment.
 // ------------------------------------------------------------------------
+constexpr int kMaxStages = 8;
+
+struct TcShape {
+  int BN, xr, sw, sx;  // vocab tile, X rows per stage, lm_head stages, X stages
+};
+
 template <int BN>
-__global__ void __launch_bounds__(192, 1) verify_tc_kernel(const __grid_constant__ CUtensorMap tma_x,
+__global__ void __launch_bounds__(224, 1) verify_tc_kernel(const __grid_constant__ CUtensorMap tma_x,
                                                           const __grid_constant__ CUtensorMap tma_w, int H,
-                                                          int n_mt, EpiArgs ea) {
+                                                          int n_mt, TcShape sh, EpiArgs ea) {
   extern __shared__ __align__(1024) unsigned char tc_smem_raw[];
-  constexpr uint32_t A_BYTES = BM * BK * 2;
-  constexpr uint32_t B_BYTES = BN * BK * 2;
-  constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
+  const uint32_t X_BYTES = static_cast<uint32_t>(sh.xr) * BK * 2;
+  constexpr uint32_t W_BYTES = BN * BK * 2;
   constexpr uint32_t TMEM_COLS = BN <= 32 ? 32 : BN <= 64 ? 64 : BN <= 128 ? 128 : 256;
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(tc_smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
-  uint64_t* empty = full + STAGES;
-  uint64_t* accb = empty + STAGES;
+  unsigned char* xsm = smem;                                  // [sx][xr rows x 128 B]
+  unsigned char* wsm = smem + sh.sx * X_BYTES;                // [sw][BN rows x 128 B]
+  uint64_t* wfull = reinterpret_cast<uint64_t*>(wsm + sh.sw * W_BYTES);
+  uint64_t* wempty = wfull + kMaxStages;
+  uint64_t* xfull = wempty + kMaxStages;
+  uint64_t* xempty = xfull + kMaxStages;
+  uint64_t* accb = xempty + kMaxStages;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accb + 1);
   __shared__ int s_fail;
 
@@ -150,12 +177,18 @@ __global__ void __launch_bounds__(192, 1) verify_tc_kernel(const __grid_constant
   const int m_t = tile % n_mt, n_t = tile / n_mt;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nk = cdiv(H, BK);
+  const int rot = static_cast<int>(static_cast<long>(blockIdx.x) * nk / gridDim.x);
+  auto kblock = [&](int i) { const int k = i + rot; return k >= nk ? k - nk : k; };
 
   if (threadIdx.x == 0) {
     s_fail = 0;
-    for (int s = 0; s < STAGES; ++s) {
-      tc::mbar_init(full + s, 1);
-      tc::mbar_init(empty + s, 1);
+    for (int s = 0; s < sh.sw; ++s) {
+      tc::mbar_init(wfull + s, 1);
+      tc::mbar_init(wempty + s, 1);
+    }
+    for (int s = 0; s < sh.sx; ++s) {
+      tc::mbar_init(xfull + s, 1);
+      tc::mbar_init(xempty + s, 1);
     }
     tc::mbar_init(accb, 1);
     tc::fence_mbar_init();
@@ -168,39 +201,53 @@ __global__ void __launch_bounds__(192, 1) verify_tc_kernel(const __grid_constant
   const uint32_t taddr = *tmem_slot;
 
   if (warp == 4) {
+    // lm_head is a constant input of the step: its stream starts before the
+    // wait on the preceding kernel
     if (lane == 0) {
-      for (int kb = 0; kb < nk; ++kb) {
-        const int s = kb % STAGES;
-        const uint32_t ph = (kb / STAGES) & 1;
-        if (!tc::mbar_wait(empty + s, ph ^ 1)) { s_fail = 1; break; }
-        const uint32_t sa = smem_u32(smem + s * STAGE_BYTES);
-        tc::mbar_expect_tx(full + s, STAGE_BYTES);
-        tc::tma_load_2d(sa, &tma_x, kb * BK, m_t * BM, full + s);
-        tc::tma_load_2d(sa + A_BYTES, &tma_w, kb * BK, n_t * BN, full + s);
+      for (int i = 0; i < nk; ++i) {
+        const int s = i % sh.sw;
+        const uint32_t ph = (i / sh.sw) & 1;
+        if (!tc::mbar_wait(wempty + s, ph ^ 1)) { s_fail = 1; break; }
+        tc::mbar_expect_tx(wfull + s, W_BYTES);
+        tc::tma_load_2d(smem_u32(wsm + s * W_BYTES), &tma_w, kblock(i) * BK, n_t * BN, wfull + s);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 6) {
+    pdl_wait();
+    if (lane == 0) {
+      for (int i = 0; i < nk; ++i) {
+        const int s = i % sh.sx;
+        const uint32_t ph = (i / sh.sx) & 1;
+        if (!tc::mbar_wait(xempty + s, ph ^ 1)) { s_fail = 1; break; }
+        tc::mbar_expect_tx(xfull + s, X_BYTES);
+        tc::tma_load_2d(smem_u32(xsm + s * X_BYTES), &tma_x, kblock(i) * BK, m_t * BM, xfull + s);
       }
     }
     __syncwarp();
   } else if (warp == 5) {
     if (lane == 0) {
       constexpr uint32_t idesc = tc::idesc_bf16_f32(BM, BN);
-      for (int kb = 0; kb < nk; ++kb) {
-        const int s = kb % STAGES;
-        const uint32_t ph = (kb / STAGES) & 1;
-        if (!tc::mbar_wait(full + s, ph)) { s_fail = 1; break; }
-        tc::fence_after_sync();
-        const uint32_t sa = smem_u32(smem + s * STAGE_BYTES);
-#pragma unroll
-        for (int k = 0; k < BK / 16; ++k) {
-          const uint64_t ad = tc::smem_desc_sw128(sa + k * 32);
-          const uint64_t bd = tc::smem_desc_sw128(sa + A_BYTES + k * 32);
-          tc::mma_bf16(taddr, ad, bd, idesc, (kb | k) != 0);
+      for (int i = 0; i < nk; ++i) {
+        const int sw = i % sh.sw, sx = i % sh.sx;
+        if (!tc::mbar_wait(wfull + sw, (i / sh.sw) & 1) || !tc::mbar_wait(xfull + sx, (i / sh.sx) & 1)) {
+          s_fail = 1;
+          break;
         }
-        tc::mma_commit(empty + s);
+        tc::fence_after_sync();
+        const uint32_t sa = smem_u32(xsm + sx * X_BYTES), sb = smem_u32(wsm + sw * W_BYTES);
+#pragma unroll
+        for (int k = 0; k < BK / 16; ++k)
+          tc::mma_bf16(taddr, tc::smem_desc_sw128(sa + k * 32), tc::smem_desc_sw128(sb + k * 32), idesc,
+                       (i | k) != 0);
+        tc::mma_commit(wempty + sw);
+        tc::mma_commit(xempty + sx);
       }
       tc::mma_commit(accb);  // fires once every issued MMA has completed
     }
     __syncwarp();
   } else {
+    pdl_wait();
     // ---- epilogue: thread = one tree-node row of this tile ----
     const bool ok = tc::mbar_wait(accb, 0);
     tc::fence_after_sync();
@@ -288,6 +335,7 @@ __global__ void __launch_bounds__(kThreads) verify_gemv_f32_kernel(const float* 
                                                                    int H, int V, int groups, float* __restrict__ z) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   float* xs = reinterpret_cast<float*>(smem_raw);
+  pdl_wait();
   stage_rows(xs, x + static_cast<size_t>(r0) * H, H, nb, H);
   __syncthreads();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -309,6 +357,7 @@ __global__ void __launch_bounds__(kThreads) verify_gemv_f32_kernel(const float* 
 __global__ void __launch_bounds__(256) verify_stats_kernel(const float* __restrict__ z, EpiArgs ea) {
   const int t = blockIdx.x, r = blockIdx.y;
   const int n0 = t * F32_TILE;
+  pdl_wait();
   const int col = n0 + threadIdx.x;
   const float v = col < ea.V ? z[static_cast<size_t>(r) * ea.V + col] : -INFINITY;
   __shared__ float sm[8];
@@ -360,6 +409,7 @@ __global__ void __launch_bounds__(256) verify_merge_kernel(const float4* __restr
                                                            float inv_tau, float4* __restrict__ rowst) {
   const int r = blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
+  pdl_wait();
   if (r >= R) return;
   const float4* pr = part + static_cast<size_t>(r) * n_nt;
   float m = -INFINITY;
@@ -408,6 +458,7 @@ __global__ void __launch_bounds__(256) accept_kernel(medusa_tree_dev tr, const i
   const int T = tr.T;
   const size_t base = static_cast<size_t>(b) * T;
   if (threadIdx.x == 0) { s_best = 0; s_path = 0x7fffffff; s_nan = 0; }
+  pdl_wait();
   for (int c = threadIdx.x; c < T; c += blockDim.x) {
     const float4 own = rowst[base + c];
     if (node_H) {
@@ -455,27 +506,54 @@ __global__ void __launch_bounds__(256) accept_kernel(medusa_tree_dev tr, const i
     if ((tr.mask[static_cast<size_t>(leaf) * tr.mask_words + best / 32] >> (best % 32)) & 1u) atomicMin(&s_path, p);
   }
   __syncthreads();
+  // accepted tokens root..best, read off best's ancestor-mask row
+  const int a_len = tr.depth[best];
+  int32_t* out = accepted_tokens + static_cast<size_t>(b) * (tr.dmax + 1);
+  for (int t = threadIdx.x; t < T; t += blockDim.x)
+    if ((tr.mask[static_cast<size_t>(best) * tr.mask_words + t / 32] >> (t % 32)) & 1u)
+      out[tr.depth[t]] = tokens[base + t];
+  for (int d = a_len + 1 + threadIdx.x; d <= tr.dmax; d += blockDim.x) out[d] = -1;
   if (threadIdx.x == 0) {
-    const int a = tr.depth[best];
-    accept_len[b] = a;
+    accept_len[b] = a_len;
     best_node[b] = best;
     best_path[b] = s_path;
     next_root[b] = __float_as_int(rowst[base + best].w);
-    int32_t* out = accepted_tokens + static_cast<size_t>(b) * (tr.dmax + 1);
-    for (int d = a + 1; d <= tr.dmax; ++d) out[d] = -1;
-    for (int n = best; n >= 0; n = tr.parent[n]) out[tr.depth[n]] = tokens[base + n];
     if (s_nan && dev_status) atomicOr(dev_status + b, MEDUSA_DEV_NAN);
   }
+}
+
+constexpr size_t kTcSmemMax = 227 * 1024;
+
+TcShape tc_shape(const VerifyPlan& p) {
+  TcShape sh{};
+  sh.BN = p.BN;
+  const int rows = p.n_mt == 1 ? p.R : BM;
+  sh.xr = std::min(BM, cdiv(rows, 8) * 8);
+  const size_t xb = static_cast<size_t>(sh.xr) * BK * 2, wb = static_cast<size_t>(p.BN) * BK * 2;
+  const size_t fixed = 1024 + (4 * kMaxStages + 1) * 8 + 16;
+  sh.sx = 4;
+  sh.sw = static_cast<int>(std::min<size_t>(kMaxStages, (kTcSmemMax - fixed - sh.sx * xb) / wb));
+  return sh;
+}
+
+size_t tc_smem_bytes(const TcShape& sh) {
+  return 1024 + static_cast<size_t>(sh.sx) * sh.xr * BK * 2 + static_cast<size_t>(sh.sw) * sh.BN * BK * 2 +
+         (4 * kMaxStages + 1) * 8 + 16;
 }
 
 template <int BN>
 int launch_tc(const VerifyPlan& p, const CUtensorMap& mx, const CUtensorMap& mw, int H, const EpiArgs& ea,
               cudaStream_t st) {
-  const size_t smem = 1024 + STAGES * (static_cast<size_t>(BM) * BK * 2 + static_cast<size_t>(BN) * BK * 2) + 256;
+  const TcShape sh = tc_shape(p);
+  if (sh.sw < 2) return MEDUSA_ERR_UNSUPPORTED;
+  const size_t smem = tc_smem_bytes(sh);
   auto k = verify_tc_kernel<BN>;
   if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) != cudaSuccess)
     return MEDUSA_ERR_CUDA;
-  k<<<p.n_mt * p.n_nt, 192, smem, st>>>(mx, mw, H, p.n_mt, ea);
+  if (launch_pdl(k, dim3(p.n_mt * p.n_nt), dim3(224), smem, st, mx, mw, H, p.n_mt, sh, ea) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return MEDUSA_ERR_CUDA;
+  }
   MEDUSA_LAUNCH_CHECK();
   return MEDUSA_OK;
 }
@@ -530,7 +608,8 @@ MEDUSA_API int medusa_verify_accept(const medusa_tree* tree, const void* x, cons
 
   if (dtype == MEDUSA_BF16) {
     CUtensorMap mx, mw;
-    if (!make_tmap_bf16(&mx, x, p.R, H, BM) || !make_tmap_bf16(&mw, lm_head, V, H, p.BN)) return MEDUSA_ERR_CUDA;
+    if (!make_tmap_bf16(&mx, x, p.R, H, tc_shape(p).xr) || !make_tmap_bf16(&mw, lm_head, V, H, p.BN))
+      return MEDUSA_ERR_CUDA;
     const int rc = dispatch_tc(p, mx, mw, H, ea, st);
     if (rc != MEDUSA_OK) return rc;
   } else {
@@ -547,18 +626,33 @@ MEDUSA_API int medusa_verify_accept(const medusa_tree* tree, const void* x, cons
       auto k = nb <= 4 ? verify_gemv_f32_kernel<4> : nb <= 8 ? verify_gemv_f32_kernel<8> : verify_gemv_f32_kernel<16>;
       if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) != cudaSuccess)
         return MEDUSA_ERR_CUDA;
-      k<<<ctas, kThreads, smem, st>>>(static_cast<const float*>(x), static_cast<const float*>(lm_head), r0, nb, H,
-                                      V, groups, z);
+      if (launch_pdl(k, dim3(ctas), dim3(kThreads), smem, st, static_cast<const float*>(x),
+                     static_cast<const float*>(lm_head), r0, nb, H, V, groups, z) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return MEDUSA_ERR_CUDA;
+      }
       MEDUSA_LAUNCH_CHECK();
     }
-    verify_stats_kernel<<<dim3(p.n_nt, p.R), 256, 0, st>>>(z, ea);
+    if (launch_pdl(verify_stats_kernel, dim3(p.n_nt, p.R), dim3(256), 0, st, static_cast<const float*>(z), ea) !=
+        cudaSuccess) {
+      (void)cudaGetLastError();
+      return MEDUSA_ERR_CUDA;
+    }
     MEDUSA_LAUNCH_CHECK();
   }
-  verify_merge_kernel<<<cdiv(p.R, 8), 256, 0, st>>>(w.part, p.R, p.n_nt, inv_tau, w.rowst);
+  if (launch_pdl(verify_merge_kernel, dim3(cdiv(p.R, 8)), dim3(256), 0, st, static_cast<const float4*>(w.part), p.R,
+                 p.n_nt, inv_tau, w.rowst) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return MEDUSA_ERR_CUDA;
+  }
   MEDUSA_LAUNCH_CHECK();
-  accept_kernel<<<B, 256, T, st>>>(tree->dev, tree_tokens, w.rowst, w.child_z, inv_tau, posterior_threshold,
-                                   posterior_alpha, node_p, node_H, accept_len, best_path, best_node, accepted_tokens,
-                                   next_root, dev_status);
+  if (launch_pdl(accept_kernel, dim3(B), dim3(256), static_cast<size_t>(T), st, tree->dev, tree_tokens,
+                 static_cast<const float4*>(w.rowst), static_cast<const float*>(w.child_z), inv_tau,
+                 posterior_threshold, posterior_alpha, node_p, node_H, accept_len, best_path, best_node,
+                 accepted_tokens, next_root, dev_status) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return MEDUSA_ERR_CUDA;
+  }
   MEDUSA_LAUNCH_CHECK();
   return MEDUSA_OK;
 }
