@@ -139,25 +139,88 @@ struct EpiArgs {
 
 // ------------------------------------------------------------------------
 // K5, bf16: tcgen05 GEMM with the statistics epilogue.
-// 224 threads: warps 0-3 epilogue (TMEM lanes 0-127), warp 4 streams lm_head
-// tiles, warp 5 issues the MMAs and owns TMEM, warp 6 streams the tree rows X.
+// 352 threads: warps 0-7 epilogue (warp w reads TMEM lanes 32*(w%4).. and
+// the (w/4)-th half of the tile's columns), warp 8 streams lm_head tiles,
+// warp 9 issues the MMAs and owns TMEM, warp 10 streams the tree rows X.
 // lm_head (from HBM) and X (from L2, shared by every CTA) run in separate
 // rings: a deep one for the weight stream, a shallow one for X, whose stage
 // holds only the xr rows the tile has (xr <= 128; the MMA's reads of rows
 // xr..127 land in the next stage's bytes and only feed accumulator rows that
-// are never read).  Each CTA starts its k loop at its own offset so the CTAs
-// do not all read the same block of X at the same moment.
+// are never read).
 // ------------------------------------------------------------------------
 constexpr int kMaxStages = 8;
+constexpr int kEpiWarps = 8;
+constexpr int kWarpW = kEpiWarps, kWarpMma = kEpiWarps + 1, kWarpX = kEpiWarps + 2;
+constexpr int kTcThreads = (kEpiWarps + 3) * 32;
+constexpr size_t kHalfXchgBytes = BM * 5 * 4;  // per-row statistics of the upper column half
 
 struct TcShape {
   int BN, xr, sw, sx;  // vocab tile, X rows per stage, lm_head stages, X stages
 };
 
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+// Running statistics of one row over a 32-column chunk v[0..nv): maximum and
+// its first column (tree reduction), then, at temperature > 0, the sums
+// s = sum 2^y2 and w2 = sum 2^y2 * y2 with y2 = (z - m) * k2, k2 = log2(e) /
+// temperature, rescaled when the maximum grows.  NaN never wins the maximum.
+__device__ inline void chunk_stats(const float (&v)[32], int nv, int col0, float k2, bool tempered, float& m,
+                                   int& arg, float& s, float& w2, bool& nan_seen) {
+  float t[32];
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    const bool in = j < nv;
+    nan_seen |= in && v[j] != v[j];
+    t[j] = (in && v[j] == v[j]) ? v[j] : -INFINITY;
+  }
+  float tv[16];
+  int ti[16];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    const bool take = t[j + 16] > t[j];
+    tv[j] = take ? t[j + 16] : t[j];
+    ti[j] = take ? j + 16 : j;
+  }
+#pragma unroll
+  for (int h = 8; h >= 1; h >>= 1) {
+#pragma unroll
+    for (int j = 0; j < h; ++j) {
+      const bool take = tv[j + h] > tv[j];
+      tv[j] = take ? tv[j + h] : tv[j];
+      ti[j] = take ? ti[j + h] : ti[j];
+    }
+  }
+  const float cm = tv[0];
+  if (cm > m) {
+    if (tempered && s > 0.f) {
+      const float d2 = (m - cm) * k2;
+      const float sc = exp2f(d2);
+      w2 = sc * fmaf(d2, s, w2);
+      s *= sc;
+    }
+    m = cm;
+    arg = col0 + ti[0];
+  }
+  if (tempered && m != -INFINITY) {
+    const float b2 = -m * k2;
+    float s4[4] = {0.f, 0.f, 0.f, 0.f}, w4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      const float y2 = fmaf(t[j], k2, b2);
+      const float e = exp2f(y2);  // 0 for masked (-inf) columns
+      s4[j & 3] += e;
+      w4[j & 3] = fmaf(e, e > 0.f ? y2 : 0.f, w4[j & 3]);
+    }
+    s += (s4[0] + s4[1]) + (s4[2] + s4[3]);
+    w2 += (w4[0] + w4[1]) + (w4[2] + w4[3]);
+  }
+}
+
 template <int BN>
-__global__ void __launch_bounds__(224, 1) verify_tc_kernel(const __grid_constant__ CUtensorMap tma_x,
-                                                          const __grid_constant__ CUtensorMap tma_w, int H,
-                                                          int n_mt, TcShape sh, EpiArgs ea) {
+__global__ void __launch_bounds__(kTcThreads, 1) verify_tc_kernel(const __grid_constant__ CUtensorMap tma_x,
+                                                                 const __grid_constant__ CUtensorMap tma_w, int H,
+                                                                 int n_mt, TcShape sh, EpiArgs ea) {
   extern __shared__ __align__(1024) unsigned char tc_smem_raw[];
   const uint32_t X_BYTES = static_cast<uint32_t>(sh.xr) * BK * 2;
   constexpr uint32_t W_BYTES = BN * BK * 2;
@@ -171,14 +234,13 @@ __global__ void __launch_bounds__(224, 1) verify_tc_kernel(const __grid_constant
   uint64_t* xempty = xfull + kMaxStages;
   uint64_t* accb = xempty + kMaxStages;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accb + 1);
+  float* xh = reinterpret_cast<float*>(tmem_slot + 4);        // [5][BM] upper-half row statistics
   __shared__ int s_fail;
 
   const int tile = blockIdx.x;
   const int m_t = tile % n_mt, n_t = tile / n_mt;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nk = cdiv(H, BK);
-  const int rot = static_cast<int>(static_cast<long>(blockIdx.x) * nk / gridDim.x);
-  auto kblock = [&](int i) { const int k = i + rot; return k >= nk ? k - nk : k; };
 
   if (threadIdx.x == 0) {
     s_fail = 0;
@@ -195,12 +257,12 @@ __global__ void __launch_bounds__(224, 1) verify_tc_kernel(const __grid_constant
     tc::prefetch_tmap(&tma_x);
     tc::prefetch_tmap(&tma_w);
   }
-  if (warp == 5) tc::tmem_alloc(tmem_slot, TMEM_COLS);
+  if (warp == kWarpMma) tc::tmem_alloc(tmem_slot, TMEM_COLS);
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t taddr = *tmem_slot;
 
-  if (warp == 4) {
+  if (warp == kWarpW) {
     // lm_head is a constant input of the step: its stream starts before the
     // wait on the preceding kernel
     if (lane == 0) {
@@ -209,11 +271,11 @@ __global__ void __launch_bounds__(224, 1) verify_tc_kernel(const __grid_constant
         const uint32_t ph = (i / sh.sw) & 1;
         if (!tc::mbar_wait(wempty + s, ph ^ 1)) { s_fail = 1; break; }
         tc::mbar_expect_tx(wfull + s, W_BYTES);
-        tc::tma_load_2d(smem_u32(wsm + s * W_BYTES), &tma_w, kblock(i) * BK, n_t * BN, wfull + s);
+        tc::tma_load_2d(smem_u32(wsm + s * W_BYTES), &tma_w, i * BK, n_t * BN, wfull + s);
       }
     }
     __syncwarp();
-  } else if (warp == 6) {
+  } else if (warp == kWarpX) {
     pdl_wait();
     if (lane == 0) {
       for (int i = 0; i < nk; ++i) {
@@ -221,11 +283,11 @@ __global__ void __launch_bounds__(224, 1) verify_tc_kernel(const __grid_constant
         const uint32_t ph = (i / sh.sx) & 1;
         if (!tc::mbar_wait(xempty + s, ph ^ 1)) { s_fail = 1; break; }
         tc::mbar_expect_tx(xfull + s, X_BYTES);
-        tc::tma_load_2d(smem_u32(xsm + s * X_BYTES), &tma_x, kblock(i) * BK, m_t * BM, xfull + s);
+        tc::tma_load_2d(smem_u32(xsm + s * X_BYTES), &tma_x, i * BK, m_t * BM, xfull + s);
       }
     }
     __syncwarp();
-  } else if (warp == 5) {
+  } else if (warp == kWarpMma) {
     if (lane == 0) {
       constexpr uint32_t idesc = tc::idesc_bf16_f32(BM, BN);
       for (int i = 0; i < nk; ++i) {
@@ -248,46 +310,62 @@ __global__ void __launch_bounds__(224, 1) verify_tc_kernel(const __grid_constant
     __syncwarp();
   } else {
     pdl_wait();
-    // ---- epilogue: thread = one tree-node row of this tile ----
-    const bool ok = tc::mbar_wait(accb, 0);
-    tc::fence_after_sync();
-    const int row = warp * 32 + lane;
+    // ---- epilogue: thread = one tree-node row, one half of the tile's columns ----
+    const int quad = warp & 3, half = warp >> 2;
+    const int row = quad * 32 + lane;
     const int r = m_t * BM + row;
     const bool valid_row = r < ea.R;
-    const uint32_t tl = taddr + (static_cast<uint32_t>(warp * 32) << 16);
+    const uint32_t tl = taddr + (static_cast<uint32_t>(quad * 32) << 16);
     const int n0 = n_t * BN;
-    float m = -INFINITY;
-    int arg = n0;
-    bool nan_seen = false;
-    int b = 0, node = 0, c_beg = 0, c_cnt = 0;
+    const int ncol = min(BN, ea.V - n0);  // valid columns of this tile
+    constexpr int NCH = (BN + 31) / 32;
+    const int ch0 = half ? (NCH + 1) / 2 : 0, ch1 = half ? NCH : (NCH + 1) / 2;
+    // While the MMAs run: which of this row's children have their token in
+    // this half's columns (bit k: child c_beg + k; a node has < 64 children).
+    int b = 0, c_beg = 0;
+    uint64_t hits = 0;
     if (valid_row) {
       b = r / ea.T;
-      node = r % ea.T;
+      const int node = r % ea.T;
       c_beg = ea.tr.child_start[node];
-      c_cnt = ea.tr.child_count[node];
+      const int c_cnt = ea.tr.child_count[node];
+      const int32_t* tok = ea.tokens + static_cast<size_t>(b) * ea.T + c_beg;
+      const int lo = n0 + ch0 * 32, hi = n0 + min(ncol, ch1 * 32);
+      for (int k0 = 0; k0 < c_cnt; k0 += 8) {
+        int t[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) t[u] = k0 + u < c_cnt ? tok[k0 + u] : -1;
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          if (t[u] >= lo && t[u] < hi) hits |= 1ull << (k0 + u);
+      }
     }
+    const bool ok = tc::mbar_wait(accb, 0);
+    tc::fence_after_sync();
+    const bool tempered = ea.inv_tau > 0.f;
+    const float k2 = ea.inv_tau * kLog2e;
+    float m = -INFINITY, s = 0.f, w2 = 0.f;
+    int arg = n0 + ch0 * 32;
+    bool nan_seen = false;
 #pragma unroll 1
-    for (int c0 = 0; c0 < BN; c0 += 32) {
+    for (int ch = ch0; ch < ch1; ++ch) {
+      const int c0 = ch * 32;
       float v[32];
       tc::tmem_ld32(tl + c0, v);
       if (!valid_row || !ok) continue;
-#pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        const int col = n0 + c0 + j;
-        if (c0 + j < BN && col < ea.V) {
-          if (v[j] > m) { m = v[j]; arg = col; }
-          nan_seen |= v[j] != v[j];
-        }
-      }
+      const int nv = min(32, ncol - c0);
+      chunk_stats(v, nv, n0 + c0, k2, tempered, m, arg, s, w2, nan_seen);
       if (ea.logits) {
         float* dst = ea.logits + static_cast<size_t>(r) * ea.V + n0 + c0;
 #pragma unroll
         for (int j = 0; j < 32; ++j)
-          if (c0 + j < BN && n0 + c0 + j < ea.V) dst[j] = v[j];
+          if (j < nv) dst[j] = v[j];
       }
-      for (int c = c_beg; c < c_beg + c_cnt; ++c) {
+      for (uint64_t hm = hits; hm; hm &= hm - 1) {
+        const int k = __ffsll(static_cast<long long>(hm)) - 1;
+        const int c = c_beg + k;
         const int rel = ea.tokens[static_cast<size_t>(b) * ea.T + c] - (n0 + c0);
-        if (rel >= 0 && rel < 32 && c0 + rel < BN) {
+        if (rel >= 0 && rel < nv) {
           float z = 0.f;
 #pragma unroll
           for (int j = 0; j < 32; ++j) z = (j == rel) ? v[j] : z;
@@ -295,33 +373,43 @@ __global__ void __launch_bounds__(224, 1) verify_tc_kernel(const __grid_constant
         }
       }
     }
-    float s = 0.f, w = 0.f;
-    if (ea.inv_tau > 0.f) {
-#pragma unroll 1
-      for (int c0 = 0; c0 < BN; c0 += 32) {
-        float v[32];
-        tc::tmem_ld32(tl + c0, v);
-        if (!valid_row || !ok) continue;
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          if (c0 + j < BN && n0 + c0 + j < ea.V) {
-            const float y = (v[j] - m) * ea.inv_tau;
-            const float e = expf(y);
-            s += e;
-            w = fmaf(e, y, w);
-          }
+    // the upper half hands its statistics to the lower half, which merges
+    // them (ties keep the lower column) and writes the tile's partial
+    if (half) {
+      xh[row] = m;
+      xh[BM + row] = s;
+      xh[2 * BM + row] = w2;
+      xh[3 * BM + row] = __int_as_float(arg);
+      xh[4 * BM + row] = nan_seen ? 1.f : 0.f;
+    }
+    asm volatile("bar.sync 1, %0;" ::"n"(kEpiWarps * 32) : "memory");
+    if (!half && valid_row) {
+      const float m1 = xh[row], s1 = xh[BM + row], w1 = xh[2 * BM + row];
+      const int a1 = __float_as_int(xh[3 * BM + row]);
+      nan_seen |= xh[4 * BM + row] != 0.f;
+      const float M = m1 > m ? m1 : m;
+      if (m1 > m) arg = a1;
+      float S = 0.f, W2 = 0.f;
+      if (tempered) {
+        if (s > 0.f) {
+          const float d = (m - M) * k2, sc = exp2f(d);
+          S += sc * s;
+          W2 += sc * fmaf(d, s, w2);
+        }
+        if (s1 > 0.f) {
+          const float d = (m1 - M) * k2, sc = exp2f(d);
+          S += sc * s1;
+          W2 += sc * fmaf(d, s1, w1);
         }
       }
-    }
-    if (valid_row) {
-      if (nan_seen) s = __int_as_float(0x7fc00000);
-      ea.part[static_cast<size_t>(r) * ea.n_nt + n_t] = make_float4(m, s, w, __int_as_float(arg));
+      if (nan_seen) S = __int_as_float(0x7fc00000);
+      ea.part[static_cast<size_t>(r) * ea.n_nt + n_t] = make_float4(M, S, W2 * kLn2, __int_as_float(arg));
       if ((!ok || s_fail) && ea.dev_status) atomicOr(ea.dev_status + b, MEDUSA_DEV_TIMEOUT);
     }
   }
   tc::fence_before_sync();
   __syncthreads();
-  if (warp == 5) tc::tmem_dealloc(taddr, TMEM_COLS);
+  if (warp == kWarpMma) tc::tmem_dealloc(taddr, TMEM_COLS);
 }
 
 // ------------------------------------------------------------------------
@@ -522,7 +610,8 @@ __global__ void __launch_bounds__(256) accept_kernel(medusa_tree_dev tr, const i
   }
 }
 
-constexpr size_t kTcSmemMax = 227 * 1024;
+constexpr size_t kTcSmemMax = 227 * 1024 - 1024;  // the kernel's static shared memory takes 1 KB
+constexpr size_t kTcFixedBytes = 1024 + (4 * kMaxStages + 1) * 8 + 16 + kHalfXchgBytes;
 
 TcShape tc_shape(const VerifyPlan& p) {
   TcShape sh{};
@@ -530,15 +619,13 @@ TcShape tc_shape(const VerifyPlan& p) {
   const int rows = p.n_mt == 1 ? p.R : BM;
   sh.xr = std::min(BM, cdiv(rows, 8) * 8);
   const size_t xb = static_cast<size_t>(sh.xr) * BK * 2, wb = static_cast<size_t>(p.BN) * BK * 2;
-  const size_t fixed = 1024 + (4 * kMaxStages + 1) * 8 + 16;
   sh.sx = 4;
-  sh.sw = static_cast<int>(std::min<size_t>(kMaxStages, (kTcSmemMax - fixed - sh.sx * xb) / wb));
+  sh.sw = static_cast<int>(std::min<size_t>(kMaxStages, (kTcSmemMax - kTcFixedBytes - sh.sx * xb) / wb));
   return sh;
 }
 
 size_t tc_smem_bytes(const TcShape& sh) {
-  return 1024 + static_cast<size_t>(sh.sx) * sh.xr * BK * 2 + static_cast<size_t>(sh.sw) * sh.BN * BK * 2 +
-         (4 * kMaxStages + 1) * 8 + 16;
+  return kTcFixedBytes + static_cast<size_t>(sh.sx) * sh.xr * BK * 2 + static_cast<size_t>(sh.sw) * sh.BN * BK * 2;
 }
 
 template <int BN>
@@ -550,7 +637,7 @@ int launch_tc(const VerifyPlan& p, const CUtensorMap& mx, const CUtensorMap& mw,
   auto k = verify_tc_kernel<BN>;
   if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) != cudaSuccess)
     return MEDUSA_ERR_CUDA;
-  if (launch_pdl(k, dim3(p.n_mt * p.n_nt), dim3(224), smem, st, mx, mw, H, p.n_mt, sh, ea) != cudaSuccess) {
+  if (launch_pdl(k, dim3(p.n_mt * p.n_nt), dim3(kTcThreads), smem, st, mx, mw, H, p.n_mt, sh, ea) != cudaSuccess) {
     (void)cudaGetLastError();
     return MEDUSA_ERR_CUDA;
   }
