@@ -201,8 +201,12 @@ def run_ours(args, ws, rank, local):
         one_step()
     launches_per_step = mb.kernel_launches() - n0
     S = max(1, min(args.unroll, args.steps))
-    gS = torch.cuda.CUDAGraph()
+    gS = torch.cuda.CUDAGraph()          # the timed graph: steps back to back, nothing in between
     with torch.cuda.graph(gS, stream=s):
+        for _ in range(S):
+            one_step()
+    gE = torch.cuda.CUDAGraph()          # the same steps with events between the stages
+    with torch.cuda.graph(gE, stream=s):
         for _ in range(S):
             one_step(timed_events=True)
     reps, rem = divmod(args.steps, S)
@@ -237,6 +241,13 @@ def run_ours(args, ws, rank, local):
     ms_max = float(t.item())
     status = int(step.dev_status.max().item())
 
+    # stage breakdown: a separate replay of the graph with events between the
+    # stages (an event node between two kernels stops the second one from
+    # starting before the first has finished, so these are not in the timed graph)
+    with torch.cuda.stream(s):
+        for _ in range(3):
+            gE.replay()
+    torch.cuda.synchronize()
     stage_ms = {"heads": [], "attention": [], "verify": []}
     if reps > 0:
         for e in ev_pairs:
@@ -313,7 +324,7 @@ def run_ours(args, ws, rank, local):
                    "tree_nodes": T, "q_heads": wl.Hq, "kv_heads": wl.Hkv, "head_dim": wl.D, "kv_len": wl.L,
                    "temperature": tau, "inputs": "planted accept path", "parallelism": f"replicas x{ws}",
                    "l2": "per-step working set %.2f GB > 126 MB L2; no flush" % (total_bytes / 1e9),
-                   "timing": f"CUDA graphs of {S} steps, CUDA events"},
+                   "timing": f"CUDA graphs of {S} steps, CUDA events; stage times from a separate replay with events between stages"},
         "roofline": roof,
         "step_roofline": {"bytes": total_bytes, "frac_hbm": round(total_bytes / (ms_step / 1e3) / 1e9 / hbm, 4)},
         "stages": stages,

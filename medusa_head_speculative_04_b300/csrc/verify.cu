@@ -104,6 +104,7 @@ struct VerifyWs {
   float4* part;      // [R, n_nt] (max, sum exp, sum exp*y, argmax bits)
   float* child_z;    // [R] logit of node c's token under its parent (indexed by c)
   float4* rowst;     // [R] merged statistics
+  int* tickets;      // [B] CTAs done with a request's nodes (self-resetting)
   float* zbuf;       // fp32 path: [R, V] logits when the caller gives none
   size_t bytes;
 };
@@ -113,13 +114,14 @@ VerifyWs carve_verify_ws(void* base, const VerifyPlan& p, int V, medusa_dtype dt
   size_t o = 0;
   auto take = [&](size_t n) { size_t s = o; o = align_up(o + n, 256); return s; };
   size_t op = take(static_cast<size_t>(p.R) * p.n_nt * 16), oc = take(static_cast<size_t>(p.R) * 4),
-         orow = take(static_cast<size_t>(p.R) * 16);
+         orow = take(static_cast<size_t>(p.R) * 16), otk = take(static_cast<size_t>(p.R) * 4);
   size_t oz = dt == MEDUSA_F32 ? take(static_cast<size_t>(p.R) * V * 4) : 0;
   char* c = static_cast<char*>(base);
   if (c) {
     w.part = reinterpret_cast<float4*>(c + op);
     w.child_z = reinterpret_cast<float*>(c + oc);
     w.rowst = reinterpret_cast<float4*>(c + orow);
+    w.tickets = reinterpret_cast<int*>(c + otk);
     w.zbuf = dt == MEDUSA_F32 ? reinterpret_cast<float*>(c + oz) : nullptr;
   }
   w.bytes = o;
@@ -139,9 +141,10 @@ struct EpiArgs {
 
 // ------------------------------------------------------------------------
 // K5, bf16: tcgen05 GEMM with the statistics epilogue.
-// 352 threads: warps 0-7 epilogue (warp w reads TMEM lanes 32*(w%4).. and
-// the (w/4)-th half of the tile's columns), warp 8 streams lm_head tiles,
-// warp 9 issues the MMAs and owns TMEM, warp 10 streams the tree rows X.
+// Warps 0..kEpiWarps-1 run the epilogue (warp w reads TMEM lanes 32*(w%4)..
+// and the (w/4)-th of kEpiWarps/4 column groups of the tile); the next warp
+// streams lm_head tiles, the next issues the MMAs and owns TMEM, the last
+// streams the tree rows X.
 // lm_head (from HBM) and X (from L2, shared by every CTA) run in separate
 // rings: a deep one for the weight stream, a shallow one for X, whose stage
 // holds only the xr rows the tile has (xr <= 128; the MMA's reads of rows
@@ -152,7 +155,9 @@ constexpr int kMaxStages = 8;
 constexpr int kEpiWarps = 8;
 constexpr int kWarpW = kEpiWarps, kWarpMma = kEpiWarps + 1, kWarpX = kEpiWarps + 2;
 constexpr int kTcThreads = (kEpiWarps + 3) * 32;
-constexpr size_t kHalfXchgBytes = BM * 5 * 4;  // per-row statistics of the upper column half
+constexpr int kColGroups = kEpiWarps / 4;
+constexpr size_t kHalfXchgBytes = (kColGroups - 1) * BM * 5 * 4;  // per-row statistics of groups 1..
+
 
 struct TcShape {
   int BN, xr, sw, sx;  // vocab tile, X rows per stage, lm_head stages, X stages
@@ -310,8 +315,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) verify_tc_kernel(const __grid_c
     __syncwarp();
   } else {
     pdl_wait();
-    // ---- epilogue: thread = one tree-node row, one half of the tile's columns ----
-    const int quad = warp & 3, half = warp >> 2;
+    // ---- epilogue: thread = one tree-node row, one column group of the tile ----
+    const int quad = warp & 3, grp = warp >> 2;
     const int row = quad * 32 + lane;
     const int r = m_t * BM + row;
     const bool valid_row = r < ea.R;
@@ -319,9 +324,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) verify_tc_kernel(const __grid_c
     const int n0 = n_t * BN;
     const int ncol = min(BN, ea.V - n0);  // valid columns of this tile
     constexpr int NCH = (BN + 31) / 32;
-    const int ch0 = half ? (NCH + 1) / 2 : 0, ch1 = half ? NCH : (NCH + 1) / 2;
+    const int ch0 = grp * NCH / kColGroups, ch1 = (grp + 1) * NCH / kColGroups;
     // While the MMAs run: which of this row's children have their token in
-    // this half's columns (bit k: child c_beg + k; a node has < 64 children).
+    // this group's columns (bit k: child c_beg + k; a node has < 64 children).
     int b = 0, c_beg = 0;
     uint64_t hits = 0;
     if (valid_row) {
@@ -373,22 +378,29 @@ __global__ void __launch_bounds__(kTcThreads, 1) verify_tc_kernel(const __grid_c
         }
       }
     }
-    // the upper half hands its statistics to the lower half, which merges
-    // them (ties keep the lower column) and writes the tile's partial
-    if (half) {
-      xh[row] = m;
-      xh[BM + row] = s;
-      xh[2 * BM + row] = w2;
-      xh[3 * BM + row] = __int_as_float(arg);
-      xh[4 * BM + row] = nan_seen ? 1.f : 0.f;
+    // groups 1.. hand their statistics to group 0, which merges them in
+    // column order (ties keep the lower column) and writes the tile's partial
+    if (kColGroups > 1) {
+      if (grp > 0) {
+        float* x = xh + (grp - 1) * 5 * BM;
+        x[row] = m;
+        x[BM + row] = s;
+        x[2 * BM + row] = w2;
+        x[3 * BM + row] = __int_as_float(arg);
+        x[4 * BM + row] = nan_seen ? 1.f : 0.f;
+      }
+      asm volatile("bar.sync 1, %0;" ::"n"(kEpiWarps * 32) : "memory");
     }
-    asm volatile("bar.sync 1, %0;" ::"n"(kEpiWarps * 32) : "memory");
-    if (!half && valid_row) {
-      const float m1 = xh[row], s1 = xh[BM + row], w1 = xh[2 * BM + row];
-      const int a1 = __float_as_int(xh[3 * BM + row]);
-      nan_seen |= xh[4 * BM + row] != 0.f;
-      const float M = m1 > m ? m1 : m;
-      if (m1 > m) arg = a1;
+    if (grp == 0 && valid_row) {
+      float M = m;
+      for (int g = 1; g < kColGroups; ++g) {
+        const float mg = xh[(g - 1) * 5 * BM + row];
+        if (mg > M) {
+          M = mg;
+          arg = __float_as_int(xh[(g - 1) * 5 * BM + 3 * BM + row]);
+        }
+        nan_seen |= xh[(g - 1) * 5 * BM + 4 * BM + row] != 0.f;
+      }
       float S = 0.f, W2 = 0.f;
       if (tempered) {
         if (s > 0.f) {
@@ -396,10 +408,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) verify_tc_kernel(const __grid_c
           S += sc * s;
           W2 += sc * fmaf(d, s, w2);
         }
-        if (s1 > 0.f) {
-          const float d = (m1 - M) * k2, sc = exp2f(d);
-          S += sc * s1;
-          W2 += sc * fmaf(d, s1, w1);
+        for (int g = 1; g < kColGroups; ++g) {
+          const float* x = xh + (g - 1) * 5 * BM;
+          const float mg = x[row], sg = x[BM + row], wg = x[2 * BM + row];
+          if (sg > 0.f) {
+            const float d = (mg - M) * k2, sc = exp2f(d);
+            S += sc * sg;
+            W2 += sc * fmaf(d, sg, wg);
+          }
         }
       }
       if (nan_seen) S = __int_as_float(0x7fc00000);
@@ -493,13 +509,9 @@ __global__ void __launch_bounds__(256) verify_stats_kernel(const float* __restri
 // M = max m_t; S = sum s_t e^{(m_t-M)/tau}; W = sum e^{(m_t-M)/tau} (w_t + s_t (m_t-M)/tau)
 // so that with q = softmax(z/tau): H = ln S - W / S.
 // ------------------------------------------------------------------------
-__global__ void __launch_bounds__(256) verify_merge_kernel(const float4* __restrict__ part, int R, int n_nt,
-                                                           float inv_tau, float4* __restrict__ rowst) {
-  const int r = blockIdx.x * 8 + (threadIdx.x >> 5);
+// One row's tile statistics merged by a warp, tiles in fixed order.
+__device__ inline float4 merge_row(const float4* __restrict__ pr, int n_nt, float inv_tau) {
   const int lane = threadIdx.x & 31;
-  pdl_wait();
-  if (r >= R) return;
-  const float4* pr = part + static_cast<size_t>(r) * n_nt;
   float m = -INFINITY;
   int arg = 0x7fffffff;
   for (int t = lane; t < n_nt; t += 32) {
@@ -526,54 +538,68 @@ __global__ void __launch_bounds__(256) verify_merge_kernel(const float4* __restr
     for (int t = lane; t < n_nt; t += 32) nan_seen |= pr[t].y != pr[t].y;
   }
   nan_seen = __any_sync(0xffffffffu, nan_seen);
-  if (lane == 0) rowst[r] = make_float4(m, nan_seen ? __int_as_float(0x7fc00000) : S, W, __int_as_float(arg));
+  return make_float4(m, nan_seen ? __int_as_float(0x7fc00000) : S, W, __int_as_float(arg));
 }
 
+struct AcceptArgs {
+  medusa_tree_dev tr;
+  const int32_t* tokens;
+  const float4* part;  // [R, n_nt] tile statistics
+  int n_nt, R;
+  float4* rowst;       // [R] merged statistics
+  int* tickets;        // [B] self-resetting
+  const float* child_z;
+  float inv_tau, thr, alpha;
+  float* node_p;
+  float* node_H;
+  int32_t* accept_len;
+  int32_t* best_path;
+  int32_t* best_node;
+  int32_t* accepted_tokens;
+  int32_t* next_root;
+  int32_t* dev_status;
+};
+
 // ------------------------------------------------------------------------
-// K6b: typical acceptance, longest kept prefix, next root.  CTA = request.
+// K6b: typical acceptance of request b, longest kept prefix, next root
+// (whole CTA; the request's merged statistics are in a.rowst).
 // ------------------------------------------------------------------------
-__global__ void __launch_bounds__(256) accept_kernel(medusa_tree_dev tr, const int32_t* __restrict__ tokens,
-                                                     const float4* __restrict__ rowst,
-                                                     const float* __restrict__ child_z, float inv_tau, float thr,
-                                                     float alpha, float* __restrict__ node_p,
-                                                     float* __restrict__ node_H, int32_t* __restrict__ accept_len,
-                                                     int32_t* __restrict__ best_path, int32_t* __restrict__ best_node,
-                                                     int32_t* __restrict__ accepted_tokens,
-                                                     int32_t* __restrict__ next_root, int32_t* __restrict__ dev_status) {
-  extern __shared__ unsigned char s_acc[];  // [T] own test passed, then kept
-  __shared__ int s_best, s_path, s_nan;
-  const int b = blockIdx.x;
+__device__ void accept_request(const AcceptArgs& a, int b, unsigned char* s_acc, int* s_sc) {
+  const medusa_tree_dev& tr = a.tr;
   const int T = tr.T;
   const size_t base = static_cast<size_t>(b) * T;
+  int& s_best = s_sc[0];
+  int& s_path = s_sc[1];
+  int& s_nan = s_sc[2];
   if (threadIdx.x == 0) { s_best = 0; s_path = 0x7fffffff; s_nan = 0; }
-  pdl_wait();
+  __syncthreads();
   for (int c = threadIdx.x; c < T; c += blockDim.x) {
-    const float4 own = rowst[base + c];
-    if (node_H) {
+    const float4 own = __ldcg(a.rowst + base + c);
+    if (a.node_H) {
       float H = 0.f;
-      if (inv_tau > 0.f) H = logf(own.y) - own.z / own.y;
-      node_H[base + c] = H;
+      if (a.inv_tau > 0.f) H = logf(own.y) - own.z / own.y;
+      a.node_H[base + c] = H;
     }
     if (own.x != own.x || own.y != own.y) s_nan = 1;
     if (c == 0) {
       s_acc[0] = 1;
-      if (node_p) node_p[base] = 1.f;
+      if (a.node_p) a.node_p[base] = 1.f;
       continue;
     }
-    const float4 par = rowst[base + tr.parent[c]];
-    const int32_t tok = tokens[base + c];
-    bool a;
+    const float4 par = __ldcg(a.rowst + base + tr.parent[c]);
+    const int32_t tok = a.tokens[base + c];
+    bool acc;
     float p;
-    if (inv_tau > 0.f) {
+    if (a.inv_tau > 0.f) {
       const float H = logf(par.y) - par.z / par.y;
-      p = expf((child_z[base + c] - par.x) * inv_tau) / par.y;
-      a = p > fminf(thr, alpha * expf(-H));
+      p = expf((a.child_z[base + c] - par.x) * a.inv_tau) / par.y;
+      acc = p > fminf(a.thr, a.alpha * expf(-H));
     } else {
-      a = tok == __float_as_int(par.w);
-      p = a ? 1.f : 0.f;
+      acc = tok == __float_as_int(par.w);
+      p = acc ? 1.f : 0.f;
     }
-    s_acc[c] = a ? 1 : 0;
-    if (node_p) node_p[base + c] = p;
+    s_acc[c] = acc ? 1 : 0;
+    if (a.node_p) a.node_p[base + c] = p;
   }
   __syncthreads();
   for (int d = 1; d <= tr.dmax; ++d) {
@@ -596,17 +622,52 @@ __global__ void __launch_bounds__(256) accept_kernel(medusa_tree_dev tr, const i
   __syncthreads();
   // accepted tokens root..best, read off best's ancestor-mask row
   const int a_len = tr.depth[best];
-  int32_t* out = accepted_tokens + static_cast<size_t>(b) * (tr.dmax + 1);
+  int32_t* out = a.accepted_tokens + static_cast<size_t>(b) * (tr.dmax + 1);
   for (int t = threadIdx.x; t < T; t += blockDim.x)
     if ((tr.mask[static_cast<size_t>(best) * tr.mask_words + t / 32] >> (t % 32)) & 1u)
-      out[tr.depth[t]] = tokens[base + t];
+      out[tr.depth[t]] = a.tokens[base + t];
   for (int d = a_len + 1 + threadIdx.x; d <= tr.dmax; d += blockDim.x) out[d] = -1;
   if (threadIdx.x == 0) {
-    accept_len[b] = a_len;
-    best_node[b] = best;
-    best_path[b] = s_path;
-    next_root[b] = __float_as_int(rowst[base + best].w);
-    if (s_nan && dev_status) atomicOr(dev_status + b, MEDUSA_DEV_NAN);
+    a.accept_len[b] = a_len;
+    a.best_node[b] = best;
+    a.best_path[b] = s_path;
+    a.next_root[b] = __float_as_int(__ldcg(a.rowst + base + best).w);
+    if (s_nan && a.dev_status) atomicOr(a.dev_status + b, MEDUSA_DEV_NAN);
+  }
+  __syncthreads();
+}
+
+// ------------------------------------------------------------------------
+// K6: merge each node's tile statistics (warp per node, kMergeRows nodes per
+// CTA, tiles in fixed order); the last CTA to finish a request's nodes
+// (ticket per request) then runs that request's acceptance.
+// ------------------------------------------------------------------------
+constexpr int kMergeRows = 8;
+
+__global__ void __launch_bounds__(kMergeRows * 32) merge_accept_kernel(AcceptArgs a) {
+  extern __shared__ unsigned char s_acc[];  // [T] own test passed, then kept
+  __shared__ int s_sc[3];
+  __shared__ int s_last;
+  pdl_wait();
+  const int r0 = blockIdx.x * kMergeRows, r1 = min(a.R, r0 + kMergeRows);
+  const int r = r0 + (threadIdx.x >> 5);
+  if (r < r1) {
+    const float4 v = merge_row(a.part + static_cast<size_t>(r) * a.n_nt, a.n_nt, a.inv_tau);
+    if ((threadIdx.x & 31) == 0) a.rowst[r] = v;
+  }
+  __threadfence();
+  __syncthreads();
+  const int T = a.tr.T;
+  for (int b = r0 / T; b <= (r1 - 1) / T; ++b) {
+    const int need = ((b + 1) * T - 1) / kMergeRows - (b * T) / kMergeRows + 1;  // CTAs holding b's nodes
+    if (threadIdx.x == 0) s_last = atomicAdd(a.tickets + b, 1) == need - 1;
+    __syncthreads();
+    if (s_last) {
+      __threadfence();
+      accept_request(a, b, s_acc, s_sc);
+      if (threadIdx.x == 0) a.tickets[b] = 0;  // ready for the next launch
+    }
+    __syncthreads();
   }
 }
 
@@ -727,16 +788,11 @@ MEDUSA_API int medusa_verify_accept(const medusa_tree* tree, const void* x, cons
     }
     MEDUSA_LAUNCH_CHECK();
   }
-  if (launch_pdl(verify_merge_kernel, dim3(cdiv(p.R, 8)), dim3(256), 0, st, static_cast<const float4*>(w.part), p.R,
-                 p.n_nt, inv_tau, w.rowst) != cudaSuccess) {
-    (void)cudaGetLastError();
-    return MEDUSA_ERR_CUDA;
-  }
-  MEDUSA_LAUNCH_CHECK();
-  if (launch_pdl(accept_kernel, dim3(B), dim3(256), static_cast<size_t>(T), st, tree->dev, tree_tokens,
-                 static_cast<const float4*>(w.rowst), static_cast<const float*>(w.child_z), inv_tau,
-                 posterior_threshold, posterior_alpha, node_p, node_H, accept_len, best_path, best_node,
-                 accepted_tokens, next_root, dev_status) != cudaSuccess) {
+  AcceptArgs aa{tree->dev, tree_tokens, w.part, p.n_nt, p.R, w.rowst, w.tickets, w.child_z, inv_tau,
+                posterior_threshold, posterior_alpha, node_p, node_H, accept_len, best_path, best_node,
+                accepted_tokens, next_root, dev_status};
+  if (launch_pdl(merge_accept_kernel, dim3(cdiv(p.R, kMergeRows)), dim3(kMergeRows * 32), static_cast<size_t>(T), st,
+                 aa) != cudaSuccess) {
     (void)cudaGetLastError();
     return MEDUSA_ERR_CUDA;
   }
