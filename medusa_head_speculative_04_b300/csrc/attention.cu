@@ -48,7 +48,10 @@ AttnPlan plan_attn(int T, int B, int Hq, int Hkv, int Lmax, int hint, int sms) {
   p.G = Hq / Hkv;
   p.R = T * p.G;
   p.n_qt = cdiv(p.R, 16 * kMaxWarps);
-  p.rpt = cdiv(cdiv(p.R, p.n_qt), 16) * 16;
+  // rows per query tile: a multiple of 16 (mma.sync row blocks) and, when the
+  // group divides 128, of the group size (a tile then starts at a node)
+  const int gran = (128 % p.G == 0) ? std::max(16, p.G) : 16;
+  p.rpt = cdiv(cdiv(p.R, p.n_qt), gran) * gran;
   p.W = p.rpt / 16;
   p.ntt = cdiv(T, KB);
   p.units = B * Hkv * p.n_qt;
@@ -91,8 +94,12 @@ int sm_count() {
   return n;
 }
 
+constexpr int kMaxVisTiles = 128;  // query tiles whose tree visibility travels in the launch arguments
+
 struct AttnArgs {
   medusa_tree_dev tr;
+  int vis_known;                     // vis[] holds every query tile's visibility
+  uint64_t vis[kMaxVisTiles];
   const __nv_bfloat16* q;
   const int32_t* kv_len;
   float* out;
@@ -158,8 +165,10 @@ __device__ inline bool next_seg(long long x, long long end, int& b, const AttnAr
 }
 
 // Bit j set iff some query row of query tile qt may see a key of tree tile j
-// (OR of the ancestor-mask rows of the tile's nodes).  Whole warp.
+// (OR of the ancestor-mask rows of the tile's nodes).  Precomputed on the
+// host for up to kMaxVisTiles query tiles, else computed here.  Whole warp.
 __device__ inline uint64_t tree_tiles_visible(const AttnArgs& a, int qt) {
+  if (a.vis_known) return a.vis[qt];
   const int lane = threadIdx.x & 31;
   const int r0 = qt * a.p.rpt, r1 = min(a.p.R, r0 + a.p.rpt);
   const int n0 = r0 / a.p.G, n1 = (r1 - 1) / a.p.G;
@@ -456,6 +465,422 @@ __global__ void __launch_bounds__((kMaxWarps + 1) * 32, 1) tree_attn_kernel(
   if (fail && lane == 0 && a.dev_status) atomicOr(a.dev_status + sg.b, MEDUSA_DEV_TIMEOUT);
 }
 
+// ---------------------------------------------------------------------------
+// bf16 path on the tcgen05 tensor cores.  Same split of key tiles, same
+// partial format.  Per CTA: warps 0-3 run the softmax (thread = query row of
+// the 128-row tile), warp 4 streams Q (once per segment) and K/V tiles with
+// TMA, warp 5 issues the MMAs and owns TMEM:
+//   S = Q K^T (M 128, N 64 keys, K = D) into TMEM columns [0, 64) or
+//   [64, 128) (two buffers: S of the next tile is computed while the softmax
+//   works on this one);
+//   the softmax threads read their S row, mask it (kv_len / cached tree bits),
+//   exponentiate against a running maximum and write P (bf16) into the K half
+//   of the tile's stage, which S no longer needs;
+//   O += P V (M 128, N = D, K 64 keys; V read as an MN-major operand) into
+//   TMEM columns [128, 128 + D).
+// A softmax thread rescales its O row only when its maximum grows by more
+// than 2^8 (P stays below 256 otherwise), which random or trained scores
+// almost never need after the first tile; it then first waits for PV of the
+// previous tile to complete (nothing else can be writing O at that point).
+// ---------------------------------------------------------------------------
+constexpr int kTcStages = 2;
+constexpr int kTcThreads = 192;       // warps 0-3 softmax, 4 producer, 5 MMA
+constexpr float kRescaleLog2 = 8.f;
+
+template <int D>
+struct TcLayout {
+  static constexpr uint32_t NSUB = D / 64;
+  static constexpr uint32_t Q_BYTES = NSUB * 128 * 128;  // [NSUB][128 rows][128 B]
+  static constexpr uint32_t HALF = NSUB * 64 * 128;      // K or V: [NSUB][64 keys][128 B]
+  static constexpr uint32_t STAGE = 2 * HALF;
+  static constexpr uint32_t OFF_KV = Q_BYTES;
+  static constexpr uint32_t P_BYTES = 128 * 128;         // [128 rows][64 keys] bf16
+  // P goes into the K half of its tile's stage when that holds 128 rows
+  static constexpr bool P_IN_K = HALF >= P_BYTES;
+  static constexpr uint32_t OFF_P = OFF_KV + kTcStages * STAGE;  // two own buffers otherwise
+  static constexpr uint32_t OFF_BAR = OFF_P + (P_IN_K ? 0 : 2 * P_BYTES);
+  static constexpr uint32_t BYTES = OFF_BAR + 256;
+  static constexpr uint32_t TMEM_O = 128;                 // first O column
+  // P of the ti-th tile (stage st): the stage's K half, or buffer ti % 2
+  __device__ static uint32_t p_off(int st, int ti) { return P_IN_K ? OFF_KV + st * STAGE : OFF_P + (ti & 1) * P_BYTES; }
+};
+
+// 2^x on the special-function unit (flush-to-zero; 2^-inf = 0).
+__device__ inline float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Visible tiles of a segment (cache tiles always, tree tiles per the mask).
+__device__ inline int seg_visible_tiles(const Seg& sg, uint64_t vis) {
+  int n = 0;
+  for (int t = sg.t0; t < sg.t1; ++t) n += (t < sg.nc) || ((vis >> (t - sg.nc)) & 1ull);
+  return n;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kTcThreads) tree_attn_tc_kernel(
+    const __grid_constant__ CUtensorMap tm_kc, const __grid_constant__ CUtensorMap tm_vc,
+    const __grid_constant__ CUtensorMap tm_kt, const __grid_constant__ CUtensorMap tm_vt,
+    const __grid_constant__ CUtensorMap tm_q, AttnArgs a) {
+  using Lay = TcLayout<D>;
+  constexpr int NSUB = Lay::NSUB;
+  extern __shared__ __align__(1024) unsigned char attn_tc_smem[];
+  unsigned char* smem =
+      reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(attn_tc_smem) + 1023) & ~uintptr_t(1023));
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + Lay::OFF_BAR);
+  uint64_t* kv_full = bar;                 // [kTcStages]
+  uint64_t* kv_empty = bar + kTcStages;    // [kTcStages]
+  uint64_t* q_full = bar + 2 * kTcStages;
+  uint64_t* q_empty = q_full + 1;
+  uint64_t* s_full = q_full + 2;   // [2]: one per S buffer (tile parity)
+  uint64_t* p_full = q_full + 4;   // [2]: one per tile parity
+  uint64_t* o_full = q_full + 6;
+  uint64_t* o_free = q_full + 7;
+  uint64_t* mma_done = q_full + 8;
+  uint64_t* pv_done = q_full + 9;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(q_full + 10);
+  __shared__ int s_len[MEDUSA_MAX_BATCH];
+  __shared__ long long s_cum[MEDUSA_MAX_BATCH + 1];
+  __shared__ volatile int s_fail;
+
+  const AttnPlan& p = a.p;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    s_fail = 0;
+    for (int st = 0; st < kTcStages; ++st) {
+      tc::mbar_init(kv_full + st, 1);
+      tc::mbar_init(kv_empty + st, 1);
+    }
+    tc::mbar_init(q_full, 1);
+    tc::mbar_init(q_empty, 1);
+    tc::mbar_init(s_full, 1);
+    tc::mbar_init(s_full + 1, 1);
+    tc::mbar_init(pv_done, 1);
+    tc::mbar_init(p_full, 4);
+    tc::mbar_init(p_full + 1, 4);
+    tc::mbar_init(o_full, 1);
+    tc::mbar_init(o_free, 4);
+    tc::mbar_init(mma_done, 1);
+    tc::fence_mbar_init();
+    tc::prefetch_tmap(&tm_kc);
+    tc::prefetch_tmap(&tm_vc);
+    tc::prefetch_tmap(&tm_kt);
+    tc::prefetch_tmap(&tm_vt);
+    tc::prefetch_tmap(&tm_q);
+  }
+  if (warp == 5) tc::tmem_alloc(tmem_slot, 256);
+  pdl_wait();
+  for (int b = threadIdx.x; b < a.B; b += blockDim.x) s_len[b] = min(max(a.kv_len[b], 0), a.Lmax);
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t taddr = *tmem_slot;
+  if (threadIdx.x == 0) {
+    long long c = 0;
+    const int upb = a.Hkv * p.n_qt;
+    for (int b = 0; b < a.B; ++b) {
+      s_cum[b] = c;
+      c += static_cast<long long>(upb) * (cdiv(s_len[b], KB) + p.ntt);
+    }
+    s_cum[a.B] = c;
+  }
+  __syncthreads();
+  pdl_trigger();
+  const long long total = s_cum[a.B];
+  const long long nct = min(static_cast<long long>(gridDim.x), total);
+  const bool active_cta = blockIdx.x < nct;
+  const long long start = active_cta ? blockIdx.x * total / nct : 0;
+  const long long end = active_cta ? (blockIdx.x + 1) * total / nct : 0;
+  const int G = p.G;
+
+  if (warp == 4) {
+    // ---------------- producer (whole warp walks the segments, lane 0 issues) ----------------
+    int ti = 0, si = 0;
+    bool ok = true;
+    int b = 0;
+    Seg sg;
+    for (long long x = start; ok && next_seg(x, end, b, a, s_len, s_cum, sg); x = sg.ustart + sg.t1) {
+      const uint64_t vis = tree_tiles_visible(a, sg.qt);
+      if (seg_visible_tiles(sg, vis) == 0) continue;
+      if (lane == 0) {
+        ok = !s_fail && tc::mbar_wait(q_empty, (si & 1) ^ 1);
+        if (ok) {
+          tc::mbar_expect_tx(q_full, Lay::Q_BYTES);
+          const int node0 = sg.qt * p.rpt / G;
+#pragma unroll
+          for (int h = 0; h < NSUB; ++h)
+            tc::tma_load_3d(smem_u32(smem + h * 16384), &tm_q, 64 * h, sg.g * G, sg.b * a.T + node0, q_full);
+        }
+        for (int t = sg.t0; ok && t < sg.t1; ++t) {
+          const bool tree = t >= sg.nc;
+          const int j = t - sg.nc;
+          if (tree && !((vis >> j) & 1ull)) continue;
+          const int st = ti % kTcStages;
+          if (!tc::mbar_wait(kv_empty + st, ((ti / kTcStages) & 1) ^ 1)) { ok = false; break; }
+          tc::mbar_expect_tx(kv_full + st, Lay::STAGE);
+          const uint32_t sk = smem_u32(smem + Lay::OFF_KV + st * Lay::STAGE), sv = sk + Lay::HALF;
+#pragma unroll
+          for (int h = 0; h < NSUB; ++h) {
+            if (!tree) {
+              const int z = sg.b * a.Hkv + sg.g;
+              tc::tma_load_3d(sk + h * 8192, &tm_kc, 64 * h, t * KB, z, kv_full + st);
+              tc::tma_load_3d(sv + h * 8192, &tm_vc, 64 * h, t * KB, z, kv_full + st);
+            } else {
+              const int z = sg.b * a.T + j * KB;
+              tc::tma_load_3d(sk + h * 8192, &tm_kt, 64 * h, sg.g, z, kv_full + st);
+              tc::tma_load_3d(sv + h * 8192, &tm_vt, 64 * h, sg.g, z, kv_full + st);
+            }
+          }
+          ++ti;
+        }
+      }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      ++si;
+    }
+    if (lane == 0) {
+      // every issued copy must have landed before the CTA's shared memory goes away
+      for (int i = 0; i < min(ti, kTcStages); ++i) {
+        const int k = ti - 1 - i;
+        ok &= tc::mbar_wait(kv_full + (k % kTcStages), static_cast<uint32_t>((k / kTcStages) & 1));
+      }
+      if (si > 0) ok &= tc::mbar_wait(q_full, static_cast<uint32_t>((si - 1) & 1));
+      if (!ok) s_fail = 1;
+    }
+  } else if (warp == 5) {
+    // ---------------- MMA issuer (whole warp walks the segments, lane 0 issues) ----------------
+    constexpr uint32_t idesc_s = tc::idesc_bf16_f32(128, KB);
+    constexpr uint32_t idesc_o = tc::idesc_bf16_f32_bmn(128, D);
+    const uint32_t tS = taddr, tO = taddr + Lay::TMEM_O;
+    const uint32_t sq = smem_u32(smem);
+    int ti = 0, si = 0;
+    bool ok = true;
+    int b = 0;
+    Seg sg;
+    for (long long x = start; ok && next_seg(x, end, b, a, s_len, s_cum, sg); x = sg.ustart + sg.t1) {
+      const uint64_t vis = tree_tiles_visible(a, sg.qt);
+      const int nt = seg_visible_tiles(sg, vis);
+      if (nt == 0) continue;
+      if (lane == 0) {
+        ok = tc::mbar_wait(q_full, si & 1);
+        int npv = 0, prev = -1;
+        // O += P V for tile index `tix` (stage st)
+        auto issue_pv = [&](int st, int tix) {
+          if (!tc::mbar_wait(p_full + (tix & 1), (tix >> 1) & 1)) { ok = false; return; }
+          if (npv == 0 && si > 0 && !tc::mbar_wait(o_free, (si - 1) & 1)) { ok = false; return; }
+          tc::fence_after_sync();
+          const uint32_t sp = smem_u32(smem + Lay::p_off(st, tix));
+          const uint32_t sv = smem_u32(smem + Lay::OFF_KV + st * Lay::STAGE + Lay::HALF);
+#pragma unroll
+          for (int kk = 0; kk < KB / 16; ++kk)
+            tc::mma_bf16(tO, tc::smem_desc_sw128(sp + kk * 32), tc::smem_desc_sw128_lbo_sbo(sv + kk * 2048, 8192, 1024),
+                         idesc_o, (npv | kk) != 0);
+          tc::mma_commit(kv_empty + st);
+          tc::mma_commit(pv_done);
+          ++npv;
+        };
+        for (int k = 0; ok && k < nt; ++k) {
+          const int st = ti % kTcStages;
+          if (!tc::mbar_wait(kv_full + st, (ti / kTcStages) & 1)) { ok = false; break; }
+          // S(ti) into buffer ti % 2: the softmax of tile ti-2 is done with it
+          // (its P was waited for before PV(ti-2) was issued)
+          tc::fence_after_sync();
+          const uint32_t sk = smem_u32(smem + Lay::OFF_KV + st * Lay::STAGE);
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk)
+            tc::mma_bf16(tS + (ti & 1) * KB, tc::smem_desc_sw128(sq + (kk >> 2) * 16384 + (kk & 3) * 32),
+                         tc::smem_desc_sw128(sk + (kk >> 2) * 8192 + (kk & 3) * 32), idesc_s, kk != 0);
+          tc::mma_commit(s_full + (ti & 1));
+          if (k == nt - 1) tc::mma_commit(q_empty);
+          if (k > 0) {
+            issue_pv(prev, ti - 1);
+            if (!ok) break;
+          }
+          prev = st;
+          ++ti;
+        }
+        if (ok) issue_pv(prev, ti - 1);
+        if (ok) tc::mma_commit(o_full);
+      }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      ++si;
+    }
+    if (lane == 0) {
+      // TMEM is freed at the end: wait until every MMA issued here has completed
+      tc::mma_commit(mma_done);
+      if (!tc::mbar_wait(mma_done, 0)) ok = false;
+      if (!ok) s_fail = 1;
+    }
+    __syncwarp();
+  } else {
+    // ---------------- softmax / epilogue: thread = query row ----------------
+    const int row = threadIdx.x;  // 0..127
+    const uint32_t tl = taddr + (static_cast<uint32_t>(warp * 32) << 16);
+    int ts = 0, so = 0;
+    bool ok = true;
+    int b = 0;
+    Seg sg;
+    auto cta_of = [&](long long xx) { return static_cast<int>(((xx + 1) * nct - 1) / total); };
+    for (long long x = start; next_seg(x, end, b, a, s_len, s_cum, sg); x = sg.ustart + sg.t1) {
+      const uint64_t vis = tree_tiles_visible(a, sg.qt);
+      const int nt = ok ? seg_visible_tiles(sg, vis) : 0;
+      const int r = sg.qt * p.rpt + row;
+      const bool vrow = row < p.rpt && r < p.R;
+      const int node = vrow ? r / G : 0;
+      float m_used = -INFINITY, l = 0.f;
+      int k = 0;
+      for (int t = sg.t0; ok && t < sg.t1; ++t) {
+        const bool tree = t >= sg.nc;
+        const int j = t - sg.nc;
+        if (tree && !((vis >> j) & 1ull)) continue;
+        const int st = ts % kTcStages;
+        const int k0 = tree ? j * KB : t * KB;
+        const int vc = min(KB, (tree ? a.T : s_len[sg.b]) - k0);  // keys of this tile that exist
+        uint32_t w0 = 0xffffffffu, w1 = 0xffffffffu;
+        if (tree) {
+          const int mw = a.tr.mask_words;
+          w0 = vrow ? a.tr.mask[static_cast<size_t>(node) * mw + 2 * j] : 0u;
+          w1 = (vrow && 2 * j + 1 < mw) ? a.tr.mask[static_cast<size_t>(node) * mw + 2 * j + 1] : 0u;
+        }
+        ok = __all_sync(0xffffffffu, tc::mbar_wait(s_full + (ts & 1), (ts >> 1) & 1));
+        if (!ok) break;
+        tc::fence_after_sync();
+        float sv[64];
+        {
+          float h0[32], h1[32];
+          tc::tmem_ld32(tl + (ts & 1) * KB, h0);
+          tc::tmem_ld32(tl + (ts & 1) * KB + 32, h1);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) { sv[e] = h0[e]; sv[32 + e] = h1[e]; }
+        }
+        // keys this row keeps (existing, and visible in the tree); raw scores of
+        // the others become -inf.  Most tiles keep every key of every row.
+        uint64_t km = 0;
+        if (vrow) {
+          km = vc >= KB ? ~0ull : ((1ull << vc) - 1);
+          if (tree) km &= (static_cast<uint64_t>(w1) << 32) | w0;
+        }
+        if (!__all_sync(0xffffffffu, km == ~0ull)) {
+#pragma unroll
+          for (int e = 0; e < 64; ++e) sv[e] = ((km >> e) & 1ull) ? sv[e] : -INFINITY;
+        }
+        // tile maximum by a tree of pairwise maxima (raw scores: the scale is > 0)
+        float mx[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) mx[e] = fmaxf(sv[e], sv[e + 32]);
+#pragma unroll
+        for (int h = 16; h >= 1; h >>= 1)
+#pragma unroll
+          for (int e = 0; e < h; ++e) mx[e] = fmaxf(mx[e], mx[e + h]);
+        const float tm = mx[0] == -INFINITY ? -INFINITY : mx[0] * a.scale_log2;
+        // lazy rescale: a row moves its exponent base only when its maximum grows
+        // by more than 2^8; TMEM loads/stores are warp-collective, so the warp
+        // rescales together when any of its rows needs it (factor 1 elsewhere)
+        const bool grow = tm > m_used + kRescaleLog2 || (m_used == -INFINITY && tm > -INFINITY);
+        const bool needs_o = grow && k > 0 && m_used > -INFINITY;
+        if (__any_sync(0xffffffffu, needs_o)) {
+          // PV of the previous tile must be complete before O is rewritten
+          ok = __all_sync(0xffffffffu, tc::mbar_wait(pv_done, (ts - 1) & 1));
+          if (!ok) break;
+          tc::fence_after_sync();
+          const float al = needs_o ? exp2f(m_used - tm) : 1.f;
+#pragma unroll 1
+          for (int c = 0; c < D; c += 32) {
+            float ov[32];
+            tc::tmem_ld32(tl + Lay::TMEM_O + c, ov);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) ov[e] *= al;
+            tc::tmem_st32(tl + Lay::TMEM_O + c, ov);
+          }
+          tc::tmem_st_wait();
+          l *= al;
+        }
+        if (grow) m_used = tm;
+        // P = 2^(s * scale - m) as bf16, 128-byte swizzled, keys along K
+        unsigned char* prow = smem + Lay::p_off(st, ts) + row * 128;
+        const bool any = m_used > -INFINITY;
+        const float nb = any ? -m_used : 0.f;
+        float ps[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          uint32_t pk[4];
+#pragma unroll
+          for (int q2 = 0; q2 < 4; ++q2) {
+            float p0 = ex2_approx(fmaf(sv[c * 8 + 2 * q2], a.scale_log2, nb));
+            float p1 = ex2_approx(fmaf(sv[c * 8 + 2 * q2 + 1], a.scale_log2, nb));
+            p0 = any ? p0 : 0.f;
+            p1 = any ? p1 : 0.f;
+            ps[q2] += p0 + p1;
+            __nv_bfloat162 v2 = __floats2bfloat162_rn(p0, p1);
+            pk[q2] = *reinterpret_cast<uint32_t*>(&v2);
+          }
+          *reinterpret_cast<uint4*>(prow + ((c ^ (row & 7)) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        }
+        const float psum = (ps[0] + ps[1]) + (ps[2] + ps[3]);
+        l += psum;
+        if (vc < KB) {
+          // keys past the end may hold anything: zero their V rows (P is 0 there,
+          // and 0 times a non-finite value is NaN)
+          unsigned char* vbase = smem + Lay::OFF_KV + st * Lay::STAGE + Lay::HALF;
+          const int nrow = KB - vc, n16 = nrow * 8 * NSUB;
+          for (int e = row; e < n16; e += 128) {
+            const int h = e / (nrow * 8), rr = vc + (e / 8) % nrow, c = e % 8;
+            *reinterpret_cast<uint4*>(vbase + h * 8192 + rr * 128 + c * 16) = make_uint4(0, 0, 0, 0);
+          }
+        }
+        tc::fence_proxy_async_smem();
+        tc::fence_before_sync();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(p_full + (ts & 1));
+        ++ts;
+        ++k;
+      }
+      // ---- segment result: final rows, or a partial for the combine launch ----
+      if (nt > 0 && ok) ok = __all_sync(0xffffffffu, tc::mbar_wait(o_full, so & 1));
+      if (!ok) break;
+      const int c_first = cta_of(sg.ustart);
+      const bool whole = cta_of(sg.uend - 1) == c_first;
+      float* dst = nullptr;
+      float scale = 1.f;
+      if (whole && vrow) {
+        dst = a.out + ((static_cast<size_t>(sg.b) * a.T + node) * a.Hq + sg.g * G + r % G) * D;
+        scale = 1.f / l;
+        if (!(l > 0.f) && a.dev_status) atomicOr(a.dev_status + sg.b, MEDUSA_DEV_NAN);
+      } else if (!whole && row < p.rpt) {
+        const int slot = blockIdx.x * 2 + (start >= sg.ustart ? 0 : 1);
+        const size_t prw = static_cast<size_t>(slot) * p.rpt + row;
+        dst = a.ws.o_part + prw * D;
+        a.ws.ml_part[prw] = make_float2(m_used, l);
+      }
+      if (nt > 0) {
+        tc::fence_after_sync();
+#pragma unroll 1
+        for (int c = 0; c < D; c += 32) {
+          float ov[32];
+          tc::tmem_ld32(tl + Lay::TMEM_O + c, ov);
+          if (dst)
+#pragma unroll
+            for (int e = 0; e < 32; e += 4)
+              *reinterpret_cast<float4*>(dst + c + e) =
+                  make_float4(ov[e] * scale, ov[e + 1] * scale, ov[e + 2] * scale, ov[e + 3] * scale);
+        }
+        tc::fence_before_sync();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(o_free);
+        ++so;
+      } else if (dst) {
+        for (int e = 0; e < D; e += 4) *reinterpret_cast<float4*>(dst + e) = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    }
+    if (!ok) s_fail = 1;
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 5) tc::tmem_dealloc(taddr, 256);
+  if (threadIdx.x == 0 && s_fail && a.dev_status)
+    for (int b = 0; b < a.B; ++b) atomicOr(a.dev_status + b, MEDUSA_DEV_TIMEOUT);
+}
+
 // Merge the partials of every head that spans several CTAs: one warp per
 // (head unit, query row), parts in CTA order.  The split is recomputed from
 // kv_len exactly as the attention launch made it.
@@ -665,13 +1090,35 @@ int launch_attn_bf16(const medusa_tree* tree, const void* q, const void* k_new, 
   a.Lmax = Lmax;
   a.scale_log2 = scale * 1.4426950408889634f;
   a.p = p;
-  const size_t smem = 1024 + static_cast<size_t>(kStages) * 2 * (D / 64) * 8192 + 2 * kStages * 8;
-  auto k = tree_attn_kernel<D>;
-  if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) != cudaSuccess)
-    return MEDUSA_ERR_CUDA;
-  if (launch_pdl(k, dim3(p.nctas), dim3((p.W + 1) * 32), smem, st, kc, vc, kt, vt, a) != cudaSuccess) {
-    (void)cudaGetLastError();
-    return MEDUSA_ERR_CUDA;
+  a.vis_known = 0;
+  if (p.n_qt <= kMaxVisTiles) {
+    const std::vector<uint64_t>& v = tree_tile_visibility(const_cast<medusa_tree*>(tree), p.G, p.rpt);
+    for (int i = 0; i < p.n_qt; ++i) a.vis[i] = v[i];
+    a.vis_known = 1;
+  }
+  if (128 % p.G == 0) {
+    // tensor-core path: Q tiles of 128 rows (node, query head of the group) by TMA
+    CUtensorMap tq;
+    if (!make_tmap_bf16_3d(&tq, q, D, Hq, static_cast<uint64_t>(B) * T, rowb, static_cast<uint64_t>(Hq) * rowb, p.G,
+                           128 / p.G))
+      return MEDUSA_ERR_CUDA;
+    const size_t smem = 1024 + TcLayout<D>::BYTES;
+    auto k = tree_attn_tc_kernel<D>;
+    if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) != cudaSuccess)
+      return MEDUSA_ERR_CUDA;
+    if (launch_pdl(k, dim3(p.nctas), dim3(kTcThreads), smem, st, kc, vc, kt, vt, tq, a) != cudaSuccess) {
+      (void)cudaGetLastError();
+      return MEDUSA_ERR_CUDA;
+    }
+  } else {
+    const size_t smem = 1024 + static_cast<size_t>(kStages) * 2 * (D / 64) * 8192 + 2 * kStages * 8;
+    auto k = tree_attn_kernel<D>;
+    if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) != cudaSuccess)
+      return MEDUSA_ERR_CUDA;
+    if (launch_pdl(k, dim3(p.nctas), dim3((p.W + 1) * 32), smem, st, kc, vc, kt, vt, a) != cudaSuccess) {
+      (void)cudaGetLastError();
+      return MEDUSA_ERR_CUDA;
+    }
   }
   MEDUSA_LAUNCH_CHECK();
   const long long warps = static_cast<long long>(p.units) * p.rpt;

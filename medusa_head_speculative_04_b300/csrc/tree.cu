@@ -125,6 +125,22 @@ MEDUSA_API int medusa_tree_create(const int32_t* ranks_flat, const int32_t* lens
   return MEDUSA_OK;
 }
 
+const std::vector<uint64_t>& tree_tile_visibility(medusa_tree* t, int G, int rpt) {
+  std::lock_guard<std::mutex> lock(t->vis_mu);
+  auto key = std::make_pair(G, rpt);
+  auto it = t->vis_cache.find(key);
+  if (it != t->vis_cache.end()) return it->second;
+  const int R = t->T * G, n_qt = cdiv(R, rpt), mw = t->mask_words;
+  std::vector<uint64_t> v(n_qt, 0);
+  for (int qt = 0; qt < n_qt; ++qt) {
+    const int r0 = qt * rpt, r1 = std::min(R, r0 + rpt);
+    for (int node = r0 / G; node <= (r1 - 1) / G; ++node)
+      for (int w = 0; w < mw; ++w)
+        if (t->mask[static_cast<size_t>(node) * mw + w]) v[qt] |= 1ull << (w >> 1);
+  }
+  return t->vis_cache.emplace(key, std::move(v)).first->second;
+}
+
 MEDUSA_API int medusa_tree_get_info(const medusa_tree* t, medusa_tree_info* info) {
   if (!t || !info) return MEDUSA_ERR_INVALID_ARG;
   std::memset(info, 0, sizeof(*info));

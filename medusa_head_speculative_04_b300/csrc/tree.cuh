@@ -3,6 +3,9 @@
 
 #include <stdint.h>
 
+#include <map>
+#include <mutex>
+#include <utility>
 #include <vector>
 
 #include "common.cuh"
@@ -27,4 +30,12 @@ struct medusa_tree {
   std::vector<uint32_t> mask;
   void* dev_block = nullptr;
   medusa_tree_dev dev{};
+  // tree-tile visibility of query tiles, per (group size, rows per tile):
+  // bit j of entry qt set iff a row of query tile qt may see a key of tree tile j
+  std::mutex vis_mu;
+  std::map<std::pair<int, int>, std::vector<uint64_t>> vis_cache;
 };
+
+// Visibility masks of the query tiles of a tree for group size G and rpt rows
+// per tile (host; computed once per shape and cached in the tree).
+const std::vector<uint64_t>& tree_tile_visibility(medusa_tree* t, int G, int rpt);
