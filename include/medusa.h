@@ -34,6 +34,13 @@
  *     it); no kernel traps or asserts.
  *   - Tree-indexed tensors use the tree's canonical node order: the root,
  *     then nodes by depth, then by rank tuple.
+ *   - Kernels are launched with programmatic dependent launch: a call may
+ *     start while the previous kernel on the stream is still finishing, and
+ *     waits for it before reading anything that work could have produced.
+ *     The weights (w1, b1, w2, lm_head) are treated as constant inputs of the
+ *     step and may be streamed before that wait, so a caller that rewrites
+ *     weights on the same stream must complete that write first (an event
+ *     wait or a stream synchronisation between the write and the call).
  */
 #ifndef MEDUSA_H_
 #define MEDUSA_H_

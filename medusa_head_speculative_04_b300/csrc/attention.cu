@@ -890,6 +890,7 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(AttnArgs a, int attn_
   __shared__ long long s_cum[MEDUSA_MAX_BATCH + 1];
   const AttnPlan& p = a.p;
   pdl_wait();
+  pdl_trigger();
   for (int b = threadIdx.x; b < a.B; b += blockDim.x) s_len[b] = min(max(a.kv_len[b], 0), a.Lmax);
   __syncthreads();
   if (threadIdx.x == 0) {

@@ -27,6 +27,7 @@ __global__ void __launch_bounds__(kCommitThreads) kv_commit_kernel(
   const int b = blockIdx.x;
   const int T = tr.T, mw = tr.mask_words;
   pdl_wait();
+  pdl_trigger();
   if (threadIdx.x == 0) {
     int best = best_node[b];
     if (best < 0 || best >= T) best = 0;

@@ -186,6 +186,7 @@ __global__ void build_tree_kernel(medusa_tree_dev tr, const int32_t* __restrict_
   const int b = blockIdx.x;
   const int T = tr.T;
   pdl_wait();
+  pdl_trigger();
   const int32_t L = kv_len[b];
   const int32_t root = root_tok[b];
   bool bad = root < 0;

@@ -649,6 +649,7 @@ __global__ void __launch_bounds__(kMergeRows * 32) merge_accept_kernel(AcceptArg
   __shared__ int s_sc[3];
   __shared__ int s_last;
   pdl_wait();
+  pdl_trigger();
   const int r0 = blockIdx.x * kMergeRows, r1 = min(a.R, r0 + kMergeRows);
   const int r = r0 + (threadIdx.x >> 5);
   if (r < r1) {
