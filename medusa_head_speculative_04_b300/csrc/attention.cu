@@ -38,6 +38,7 @@ constexpr int KB = 64;          // keys per tile
 constexpr int kStages = 3;      // K/V tiles in flight per CTA
 constexpr int kCtasPerSm = 2;
 constexpr int kMaxWarps = 8;    // consumer warps: 128 query rows
+constexpr int kMaxSplit = 320;  // CTAs of a split (2 per SM, up to 160 SMs)
 
 struct AttnPlan {
   int G, R, n_qt, rpt, W, ntt, nctas, units;
@@ -57,7 +58,12 @@ AttnPlan plan_attn(int T, int B, int Hq, int Hkv, int Lmax, int hint, int sms) {
   p.units = B * Hkv * p.n_qt;
   const int L = hint > 0 ? std::min(hint, Lmax) : Lmax;
   const long total = static_cast<long>(p.units) * (cdiv(std::max(L, 0), KB) + p.ntt);
-  p.nctas = static_cast<int>(std::max(1L, std::min(static_cast<long>(kCtasPerSm) * sms, total)));
+  long n = std::min(std::min(static_cast<long>(kCtasPerSm) * sms, total), static_cast<long>(kMaxSplit));
+  // A CTA whose range crosses from one unit into the next pays a second Q load
+  // and O drain.  When every request has the same length, a grid that is a
+  // multiple of the unit count puts every split point on a unit boundary.
+  if (p.units <= n && n % p.units != 0) n = n / p.units * p.units;
+  p.nctas = static_cast<int>(std::max(1L, n));
   return p;
 }
 
@@ -138,6 +144,22 @@ __device__ inline uint32_t tile_addr(uint32_t base, int key, int chunk) {
   return base + ((chunk >> 3) << 13) + key * 128 + (((chunk & 7) ^ (key & 7)) << 4);
 }
 
+// The split of the concatenated tile sequence: CTA c takes [start[c], start[c+1])
+// with start[c] = c * total / n.  Built once per CTA in shared memory (the 64-bit
+// divisions run in parallel), then the CTA holding position x is found by a
+// binary search instead of a division.
+__device__ inline void build_split(long long* s_start, long long total, int n) {
+  for (int c = threadIdx.x; c <= n; c += blockDim.x) s_start[c] = static_cast<long long>(c) * total / n;
+}
+__device__ inline int split_cta_of(const long long* s_start, int n, long long x) {
+  int lo = 0, hi = n - 1;  // largest c with start[c] <= x
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (s_start[mid] <= x) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
 // One (request, KV head, query tile) unit met by a CTA: tiles [t0, t1) of its
 // virtual tile sequence (nc cache tiles, then the tree tiles).
 struct Seg {
@@ -198,6 +220,7 @@ __global__ void __launch_bounds__((kMaxWarps + 1) * 32, 1) tree_attn_kernel(
   uint64_t* empty = full + kStages;
   __shared__ int s_len[MEDUSA_MAX_BATCH];
   __shared__ long long s_cum[MEDUSA_MAX_BATCH + 1];
+  __shared__ long long s_start[kMaxSplit + 1];
 
   const AttnPlan& p = a.p;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -230,9 +253,11 @@ __global__ void __launch_bounds__((kMaxWarps + 1) * 32, 1) tree_attn_kernel(
   const long long total = s_cum[a.B];
   // the grid was sized from an upper bound of kv_len: with fewer tiles than
   // CTAs only the first `total` CTAs take part, so that every range is non-empty
-  const long long nct = min(static_cast<long long>(gridDim.x), total);
-  if (blockIdx.x >= nct) return;
-  const long long start = blockIdx.x * total / nct, end = (blockIdx.x + 1) * total / nct;
+  const int nct = static_cast<int>(min(static_cast<long long>(gridDim.x), total));
+  build_split(s_start, total, nct);
+  __syncthreads();
+  if (static_cast<int>(blockIdx.x) >= nct) return;
+  const long long start = s_start[blockIdx.x], end = s_start[blockIdx.x + 1];
 
   if (warp == W) {
     // ---------------- producer: TMA loads of K/V tiles ----------------
@@ -289,7 +314,7 @@ __global__ void __launch_bounds__((kMaxWarps + 1) * 32, 1) tree_attn_kernel(
   bool fail = false;
   int b = 0;
   Seg sg;
-  auto cta_of = [&](long long xx) { return static_cast<int>(((xx + 1) * nct - 1) / total); };
+  auto cta_of = [&](long long xx) { return split_cta_of(s_start, nct, xx); };
   for (long long x = start; !fail && next_seg(x, end, b, a, s_len, s_cum, sg); x = sg.ustart + sg.t1) {
     const uint64_t vis = tree_tiles_visible(a, sg.qt);
     const int row0 = sg.qt * p.rpt + warp * 16;
@@ -543,6 +568,8 @@ __global__ void __launch_bounds__(kTcThreads) tree_attn_tc_kernel(
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(q_full + 10);
   __shared__ int s_len[MEDUSA_MAX_BATCH];
   __shared__ long long s_cum[MEDUSA_MAX_BATCH + 1];
+  __shared__ long long s_start[kMaxSplit + 1];
+  __shared__ uint64_t s_vis[kMaxVisTiles];
   __shared__ volatile int s_fail;
 
   const AttnPlan& p = a.p;
@@ -571,6 +598,8 @@ __global__ void __launch_bounds__(kTcThreads) tree_attn_tc_kernel(
     tc::prefetch_tmap(&tm_q);
   }
   if (warp == 5) tc::tmem_alloc(tmem_slot, 256);
+  if (a.vis_known)
+    for (int i = threadIdx.x; i < p.n_qt; i += blockDim.x) s_vis[i] = a.vis[i];
   pdl_wait();
   for (int b = threadIdx.x; b < a.B; b += blockDim.x) s_len[b] = min(max(a.kv_len[b], 0), a.Lmax);
   __syncthreads();
@@ -588,10 +617,12 @@ __global__ void __launch_bounds__(kTcThreads) tree_attn_tc_kernel(
   __syncthreads();
   pdl_trigger();
   const long long total = s_cum[a.B];
-  const long long nct = min(static_cast<long long>(gridDim.x), total);
-  const bool active_cta = blockIdx.x < nct;
-  const long long start = active_cta ? blockIdx.x * total / nct : 0;
-  const long long end = active_cta ? (blockIdx.x + 1) * total / nct : 0;
+  const int nct = static_cast<int>(min(static_cast<long long>(gridDim.x), total));
+  build_split(s_start, total, nct);
+  __syncthreads();
+  const bool active_cta = static_cast<int>(blockIdx.x) < nct;
+  const long long start = active_cta ? s_start[blockIdx.x] : 0;
+  const long long end = active_cta ? s_start[blockIdx.x + 1] : 0;
   const int G = p.G;
 
   if (warp == 4) {
@@ -601,7 +632,7 @@ __global__ void __launch_bounds__(kTcThreads) tree_attn_tc_kernel(
     int b = 0;
     Seg sg;
     for (long long x = start; ok && next_seg(x, end, b, a, s_len, s_cum, sg); x = sg.ustart + sg.t1) {
-      const uint64_t vis = tree_tiles_visible(a, sg.qt);
+      const uint64_t vis = (a.vis_known ? s_vis[sg.qt] : tree_tiles_visible(a, sg.qt));
       if (seg_visible_tiles(sg, vis) == 0) continue;
       if (lane == 0) {
         ok = !s_fail && tc::mbar_wait(q_empty, (si & 1) ^ 1);
@@ -658,7 +689,7 @@ __global__ void __launch_bounds__(kTcThreads) tree_attn_tc_kernel(
     int b = 0;
     Seg sg;
     for (long long x = start; ok && next_seg(x, end, b, a, s_len, s_cum, sg); x = sg.ustart + sg.t1) {
-      const uint64_t vis = tree_tiles_visible(a, sg.qt);
+      const uint64_t vis = (a.vis_known ? s_vis[sg.qt] : tree_tiles_visible(a, sg.qt));
       const int nt = seg_visible_tiles(sg, vis);
       if (nt == 0) continue;
       if (lane == 0) {
@@ -720,9 +751,9 @@ __global__ void __launch_bounds__(kTcThreads) tree_attn_tc_kernel(
     bool ok = true;
     int b = 0;
     Seg sg;
-    auto cta_of = [&](long long xx) { return static_cast<int>(((xx + 1) * nct - 1) / total); };
+    auto cta_of = [&](long long xx) { return split_cta_of(s_start, nct, xx); };
     for (long long x = start; next_seg(x, end, b, a, s_len, s_cum, sg); x = sg.ustart + sg.t1) {
-      const uint64_t vis = tree_tiles_visible(a, sg.qt);
+      const uint64_t vis = (a.vis_known ? s_vis[sg.qt] : tree_tiles_visible(a, sg.qt));
       const int nt = ok ? seg_visible_tiles(sg, vis) : 0;
       const int r = sg.qt * p.rpt + row;
       const bool vrow = row < p.rpt && r < p.R;
@@ -888,6 +919,7 @@ template <int D>
 __global__ void __launch_bounds__(256) attn_combine_kernel(AttnArgs a, int attn_ctas) {
   __shared__ int s_len[MEDUSA_MAX_BATCH];
   __shared__ long long s_cum[MEDUSA_MAX_BATCH + 1];
+  __shared__ long long s_start[kMaxSplit + 1];
   const AttnPlan& p = a.p;
   pdl_wait();
   pdl_trigger();
@@ -903,25 +935,25 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(AttnArgs a, int attn_
     s_cum[a.B] = c;
   }
   __syncthreads();
+  const long long total = s_cum[a.B];
+  const int nct = static_cast<int>(min(static_cast<long long>(attn_ctas), total));
+  build_split(s_start, total, nct);
+  __syncthreads();
   const int lane = threadIdx.x & 31;
-  const long long gw = static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  if (gw >= static_cast<long long>(p.units) * p.rpt) return;
-  const int unit = static_cast<int>(gw / p.rpt), row = static_cast<int>(gw % p.rpt);
+  const int gw = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (gw >= p.units * p.rpt) return;
+  const int unit = gw / p.rpt, row = gw % p.rpt;
   const int qt = unit % p.n_qt, g = (unit / p.n_qt) % a.Hkv, b = unit / (p.n_qt * a.Hkv);
   const int r = qt * p.rpt + row;
   if (r >= p.R) return;
-  const long long total = s_cum[a.B];
-  const long long nct = min(static_cast<long long>(attn_ctas), total);
   const int cost = cdiv(s_len[b], KB) + p.ntt;
   const long long ustart = s_cum[b] + static_cast<long long>(g * p.n_qt + qt) * cost;
-  auto cta_of = [&](long long xx) { return static_cast<int>(((xx + 1) * nct - 1) / total); };
-  const int c_first = cta_of(ustart);
-  const int nparts = cta_of(ustart + cost - 1) - c_first + 1;
+  const int c_first = split_cta_of(s_start, nct, ustart);
+  const int nparts = split_cta_of(s_start, nct, ustart + cost - 1) - c_first + 1;
   if (nparts == 1) return;  // written by the attention launch
   auto part_row = [&](int q) -> size_t {
     const int c = c_first + q;
-    const long long cs = static_cast<long long>(c) * total / nct;
-    return static_cast<size_t>(c * 2 + (cs >= ustart ? 0 : 1)) * p.rpt + row;
+    return static_cast<size_t>(c * 2 + (s_start[c] >= ustart ? 0 : 1)) * p.rpt + row;
   };
   // running max and denominator over the parts (lanes take parts)
   float M = -INFINITY;

@@ -24,14 +24,17 @@ __global__ void __launch_bounds__(kCommitThreads) kv_commit_kernel(
     int row_vecs, int Lmax, int32_t* __restrict__ dev_status) {
   __shared__ int chain[MEDUSA_MAX_DEPTH + 1];
   __shared__ int s_best, s_n, s_L;
+  extern __shared__ int16_t s_dep[];  // [T] depths: constant, read before the wait
   const int b = blockIdx.x;
   const int T = tr.T, mw = tr.mask_words;
+  for (int t = threadIdx.x; t < T; t += blockDim.x) s_dep[t] = static_cast<int16_t>(tr.depth[t]);
+  __syncthreads();
   pdl_wait();
   pdl_trigger();
   if (threadIdx.x == 0) {
     int best = best_node[b];
     if (best < 0 || best >= T) best = 0;
-    const int a = tr.depth[best];
+    const int a = s_dep[best];
     const int L = kv_len[b];
     s_best = best;
     s_L = L;
@@ -42,7 +45,7 @@ __global__ void __launch_bounds__(kCommitThreads) kv_commit_kernel(
   // the kept path root..best, by depth, read off best's ancestor-mask row
   const int best = s_best;
   for (int t = threadIdx.x; t < T; t += blockDim.x)
-    if ((tr.mask[static_cast<size_t>(best) * mw + t / 32] >> (t % 32)) & 1u) chain[tr.depth[t]] = t;
+    if ((tr.mask[static_cast<size_t>(best) * mw + t / 32] >> (t % 32)) & 1u) chain[s_dep[t]] = t;
   __syncthreads();
   const int n = s_n, L = s_L;
   if (n < 0) return;
@@ -92,7 +95,8 @@ MEDUSA_API int medusa_kv_commit(const medusa_tree* tree, const void* k_new, cons
   for (const void* q : ptrs)
     if (!aligned16(q)) return MEDUSA_ERR_ALIGNMENT;
   if (dev_status && !aligned16(dev_status)) return MEDUSA_ERR_ALIGNMENT;
-  if (launch_pdl(kv_commit_kernel, dim3(B), dim3(kCommitThreads), 0, reinterpret_cast<cudaStream_t>(stream),
+  if (launch_pdl(kv_commit_kernel, dim3(B), dim3(kCommitThreads), static_cast<size_t>(tree->T) * 2,
+                 reinterpret_cast<cudaStream_t>(stream),
                  tree->dev, static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new),
                  static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), kv_len, best_node, Hkv, D * es / 16, Lmax,
                  dev_status) != cudaSuccess) {

@@ -101,7 +101,8 @@ bool plan_heads(int B, int H, int V, int K, int with_root, int esize, int topk, 
   p.cph = cph;
   p.rpc = cdiv(V, p.cph);
   const long fc_rows = static_cast<long>(K) * H;
-  const int fc_occ = static_cast<size_t>(p.bgroup) * H * esize > kSmemTwoPerSm ? 1 : 2;
+  const size_t fc_smem = static_cast<size_t>(p.bgroup) * H * esize;
+  const int fc_occ = fc_smem > kSmemTwoPerSm ? 1 : 2;
   p.fc_ctas = static_cast<int>(std::max(1L, std::min(static_cast<long>(sms) * fc_occ, fc_rows)));
   *out = p;
   return true;
@@ -163,6 +164,10 @@ __global__ void __launch_bounds__(kThreads) heads_fc_kernel(const T* __restrict_
   constexpr int R = Pass<BMAX>::R;
   for (long row0 = w0; row0 < w1; row0 += R) {
     const int valid = w1 - row0 < R ? static_cast<int>(w1 - row0) : R;
+    // the biases of this pass load while the weight row streams in
+    float bias[R];
+#pragma unroll
+    for (int r = 0; r < R; ++r) bias[r] = r < valid ? Elem<T>::to_f(b1[row0 + r]) : 0.f;
     float acc[R][BMAX];
     gemv_rows<T, BMAX, R, Pass<BMAX>::U>(W1, row0, valid, H, xs, nb, acc);
 #pragma unroll
@@ -172,7 +177,7 @@ __global__ void __launch_bounds__(kThreads) heads_fc_kernel(const T* __restrict_
         if (r < valid && b < nb && lane == ((r * BMAX + b) & 31)) {
           const long row = row0 + r;
           const int i = static_cast<int>(row % H);
-          const float a = acc[r][b] + Elem<T>::to_f(b1[row]);
+          const float a = acc[r][b] + bias[r];
           const float silu = a / (1.0f + expf(-a));  // SiLU(a) = a * sigmoid(a)
           const float val = Elem<T>::to_f(xs[static_cast<size_t>(b) * H + i]) + silu;
           u[static_cast<size_t>(b) * nrows + row] = Elem<T>::from_f(val);

@@ -185,21 +185,30 @@ __global__ void build_tree_kernel(medusa_tree_dev tr, const int32_t* __restrict_
                                   int32_t* __restrict__ dev_status) {
   const int b = blockIdx.x;
   const int T = tr.T;
+  // depth and rank of every node: constant tables, read before the wait
+  extern __shared__ int16_t s_tab[];  // [2][T]
+  int16_t* s_dep = s_tab;
+  int16_t* s_rank = s_tab + T;
+  for (int i = threadIdx.x; i < T; i += blockDim.x) {
+    s_dep[i] = static_cast<int16_t>(tr.depth[i]);
+    s_rank[i] = static_cast<int16_t>(tr.rank[i]);
+  }
+  __syncthreads();
   pdl_wait();
   pdl_trigger();
   const int32_t L = kv_len[b];
   const int32_t root = root_tok[b];
   bool bad = root < 0;
   auto token_of = [&](int node) -> int32_t {
-    const int d = tr.depth[node];
+    const int d = s_dep[node];
     if (d == 0) return root;
-    return topk_ids[(static_cast<size_t>(b) * K + (d - 1)) * topk + tr.rank[node]];
+    return topk_ids[(static_cast<size_t>(b) * K + (d - 1)) * topk + s_rank[node]];
   };
   for (int i = threadIdx.x; i < T; i += blockDim.x) {
     const int32_t tok = token_of(i);
     bad |= tok < 0;
     tokens[static_cast<size_t>(b) * T + i] = tok;
-    pos[static_cast<size_t>(b) * T + i] = L + tr.depth[i];
+    pos[static_cast<size_t>(b) * T + i] = L + s_dep[i];
   }
   if (candidates) {
     const int W = tr.dmax + 1;
@@ -223,7 +232,8 @@ MEDUSA_API int medusa_build_tree(const medusa_tree* tree, const int32_t* root_to
   if (!aligned16(root_tok) || !aligned16(topk_ids) || !aligned16(kv_len) || !aligned16(tree_tokens) ||
       !aligned16(position_ids) || (candidates && !aligned16(candidates)) || (dev_status && !aligned16(dev_status)))
     return MEDUSA_ERR_ALIGNMENT;
-  if (launch_pdl(build_tree_kernel, dim3(B), dim3(256), 0, reinterpret_cast<cudaStream_t>(stream), tree->dev,
+  if (launch_pdl(build_tree_kernel, dim3(B), dim3(256), static_cast<size_t>(tree->T) * 4,
+                 reinterpret_cast<cudaStream_t>(stream), tree->dev,
                  root_tok, topk_ids, K, topk, kv_len, tree_tokens, position_ids, candidates, dev_status) != cudaSuccess) {
     (void)cudaGetLastError();
     return MEDUSA_ERR_CUDA;

@@ -564,7 +564,8 @@ struct AcceptArgs {
 // K6b: typical acceptance of request b, longest kept prefix, next root
 // (whole CTA; the request's merged statistics are in a.rowst).
 // ------------------------------------------------------------------------
-__device__ void accept_request(const AcceptArgs& a, int b, unsigned char* s_acc, int* s_sc) {
+__device__ void accept_request(const AcceptArgs& a, int b, unsigned char* s_acc, const int16_t* s_par,
+                               const int16_t* s_dep, int* s_sc) {
   const medusa_tree_dev& tr = a.tr;
   const int T = tr.T;
   const size_t base = static_cast<size_t>(b) * T;
@@ -586,7 +587,7 @@ __device__ void accept_request(const AcceptArgs& a, int b, unsigned char* s_acc,
       if (a.node_p) a.node_p[base] = 1.f;
       continue;
     }
-    const float4 par = __ldcg(a.rowst + base + tr.parent[c]);
+    const float4 par = __ldcg(a.rowst + base + s_par[c]);
     const int32_t tok = a.tokens[base + c];
     bool acc;
     float p;
@@ -604,13 +605,13 @@ __device__ void accept_request(const AcceptArgs& a, int b, unsigned char* s_acc,
   __syncthreads();
   for (int d = 1; d <= tr.dmax; ++d) {
     for (int c = threadIdx.x; c < T; c += blockDim.x)
-      if (tr.depth[c] == d) s_acc[c] = s_acc[c] && s_acc[tr.parent[c]];
+      if (s_dep[c] == d) s_acc[c] = s_acc[c] && s_acc[s_par[c]];
     __syncthreads();
   }
   // deepest kept node, ties to the lowest canonical index
   int key = 0xFFFF;  // root: depth 0, index 0
   for (int c = threadIdx.x; c < T; c += blockDim.x)
-    if (s_acc[c]) key = max(key, (tr.depth[c] << 16) | (0xFFFF - c));
+    if (s_acc[c]) key = max(key, (static_cast<int>(s_dep[c]) << 16) | (0xFFFF - c));
   for (int o = 16; o > 0; o >>= 1) key = max(key, __shfl_xor_sync(0xffffffffu, key, o));
   if ((threadIdx.x & 31) == 0) atomicMax(&s_best, key);
   __syncthreads();
@@ -621,11 +622,11 @@ __device__ void accept_request(const AcceptArgs& a, int b, unsigned char* s_acc,
   }
   __syncthreads();
   // accepted tokens root..best, read off best's ancestor-mask row
-  const int a_len = tr.depth[best];
+  const int a_len = s_dep[best];
   int32_t* out = a.accepted_tokens + static_cast<size_t>(b) * (tr.dmax + 1);
   for (int t = threadIdx.x; t < T; t += blockDim.x)
     if ((tr.mask[static_cast<size_t>(best) * tr.mask_words + t / 32] >> (t % 32)) & 1u)
-      out[tr.depth[t]] = a.tokens[base + t];
+      out[s_dep[t]] = a.tokens[base + t];
   for (int d = a_len + 1 + threadIdx.x; d <= tr.dmax; d += blockDim.x) out[d] = -1;
   if (threadIdx.x == 0) {
     a.accept_len[b] = a_len;
@@ -645,9 +646,19 @@ __device__ void accept_request(const AcceptArgs& a, int b, unsigned char* s_acc,
 constexpr int kMergeRows = 8;
 
 __global__ void __launch_bounds__(kMergeRows * 32) merge_accept_kernel(AcceptArgs a) {
-  extern __shared__ unsigned char s_acc[];  // [T] own test passed, then kept
+  // shared: parent[T], depth[T] (int16; the tree tables are constant, so they are
+  // read before the wait on the preceding kernel), then acc[T] bytes
+  extern __shared__ __align__(16) unsigned char accept_smem[];
+  const int T = a.tr.T;
+  int16_t* s_par = reinterpret_cast<int16_t*>(accept_smem);
+  int16_t* s_dep = s_par + T;
+  unsigned char* s_acc = reinterpret_cast<unsigned char*>(s_dep + T);
   __shared__ int s_sc[3];
   __shared__ int s_last;
+  for (int c = threadIdx.x; c < T; c += blockDim.x) {
+    s_par[c] = static_cast<int16_t>(a.tr.parent[c]);
+    s_dep[c] = static_cast<int16_t>(a.tr.depth[c]);
+  }
   pdl_wait();
   pdl_trigger();
   const int r0 = blockIdx.x * kMergeRows, r1 = min(a.R, r0 + kMergeRows);
@@ -658,14 +669,13 @@ __global__ void __launch_bounds__(kMergeRows * 32) merge_accept_kernel(AcceptArg
   }
   __threadfence();
   __syncthreads();
-  const int T = a.tr.T;
   for (int b = r0 / T; b <= (r1 - 1) / T; ++b) {
     const int need = ((b + 1) * T - 1) / kMergeRows - (b * T) / kMergeRows + 1;  // CTAs holding b's nodes
     if (threadIdx.x == 0) s_last = atomicAdd(a.tickets + b, 1) == need - 1;
     __syncthreads();
     if (s_last) {
       __threadfence();
-      accept_request(a, b, s_acc, s_sc);
+      accept_request(a, b, s_acc, s_par, s_dep, s_sc);
       if (threadIdx.x == 0) a.tickets[b] = 0;  // ready for the next launch
     }
     __syncthreads();
@@ -792,8 +802,8 @@ MEDUSA_API int medusa_verify_accept(const medusa_tree* tree, const void* x, cons
   AcceptArgs aa{tree->dev, tree_tokens, w.part, p.n_nt, p.R, w.rowst, w.tickets, w.child_z, inv_tau,
                 posterior_threshold, posterior_alpha, node_p, node_H, accept_len, best_path, best_node,
                 accepted_tokens, next_root, dev_status};
-  if (launch_pdl(merge_accept_kernel, dim3(cdiv(p.R, kMergeRows)), dim3(kMergeRows * 32), static_cast<size_t>(T), st,
-                 aa) != cudaSuccess) {
+  if (launch_pdl(merge_accept_kernel, dim3(cdiv(p.R, kMergeRows)), dim3(kMergeRows * 32), static_cast<size_t>(T) * 5,
+                 st, aa) != cudaSuccess) {
     (void)cudaGetLastError();
     return MEDUSA_ERR_CUDA;
   }

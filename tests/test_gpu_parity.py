@@ -157,14 +157,16 @@ SMALL_BF16 = synth.Workload("small_bf16", 11, H=512, V=3001, K=3, Hq=8, Hkv=2, D
                             tree=("cartesian", (3, 2, 2)), ragged=(0, 300))
 SMALL_BF16_D64 = dataclasses.replace(SMALL_BF16, name="small_bf16_d64", config_id=12, D=64, Hq=4, Hkv=4,
                                      tree=("seeded", 40, (8, 4, 2)), ragged=(60, 200), B=2, V=2048)
+# a query-head group (3) that does not divide 128 takes the mma.sync attention kernel
+SMALL_BF16_G3 = dataclasses.replace(SMALL_BF16, name="small_bf16_g3", config_id=13, Hq=6, Hkv=2)
 
 
-@pytest.mark.parametrize("wl", [SMALL_BF16, SMALL_BF16_D64], ids=lambda w: w.name)
+@pytest.mark.parametrize("wl", [SMALL_BF16, SMALL_BF16_D64, SMALL_BF16_G3], ids=lambda w: w.name)
 @pytest.mark.parametrize("temperature", [0.0, 0.7])
 @pytest.mark.parametrize("variant", ["random", "plant"])
 def test_small_bf16_full_step(mb, wl, temperature, variant):
     """Ragged kv lengths (including 0), a vocabulary that is not a multiple of any tile,
-    GQA, several requests, both head dims."""
+    GQA (groups 4 and 3: both attention kernels), several requests, both head dims."""
     inp = synth.make_inputs(wl, "cuda", variant=variant)
     step, kc, vc, kl = run_step(mb, wl, inp, temperature)
     near = check_full(wl, inp, step, kc, vc, kl, temperature)
