@@ -146,6 +146,13 @@ def measured_peaks():
     return 6400.0, 1800.0, "fallback"
 
 
+def workload_config(wl, T, tau, ws):
+    """The workload keys both arms report."""
+    return {"workload": wl.name, "batch": wl.B, "hidden": wl.H, "vocab": wl.V, "heads": wl.K, "tree_nodes": T,
+            "q_heads": wl.Hq, "kv_heads": wl.Hkv, "head_dim": wl.D, "kv_len": wl.L, "temperature": tau,
+            "inputs": "planted accept path", "parallelism": f"replicas x{ws}"}
+
+
 # ----------------------------------------------------------------------------- our arm
 
 def run_ours(args, ws, rank, local):
@@ -255,39 +262,63 @@ def run_ours(args, ws, rank, local):
             stage_ms["attention"].append(e[1].elapsed_time(e[2]))
             stage_ms["verify"].append(e[2].elapsed_time(e[3]))
 
-    # end-to-end through the public API: pinned host inputs in, results out, every step
+    # end-to-end through the public API: every step copies its inputs in from
+    # pinned host memory and its results out.  The inputs of step i+1 upload on a
+    # copy stream while step i runs (two device buffers, ordered by events).
     pin = lambda x: x.detach().cpu().pin_memory()
     host_in = {k: pin(getattr(inp, k)) for k in ("h", "X", "q", "k_new", "v_new")}
     host_root = pin(root)
-    dev_in = {k: torch.empty_like(getattr(inp, k)) for k in host_in}
+    dev_bufs = [{k: torch.empty_like(getattr(inp, k)) for k in host_in} for _ in range(2)]
+    root_bufs = [torch.empty_like(root) for _ in range(2)]
     outs = (step.accept_len, step.accepted_tokens, step.next_root, step.best_node)
     host_out = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs]
     h2d = sum(v.numel() * v.element_size() for v in host_in.values()) + host_root.numel() * 4
     d2h = sum(o.numel() * o.element_size() for o in outs)
     e2e_steps = max(10, min(args.steps, 500))
+    cs = torch.cuda.Stream(dev)
+    copied = [torch.cuda.Event() for _ in range(2)]
+    consumed = [torch.cuda.Event() for _ in range(2)]
 
-    def e2e_step():
-        for k, v in host_in.items():
-            dev_in[k].copy_(v, non_blocking=True)
-        step.root.copy_(host_root, non_blocking=True)
-        kl.copy_(kv_len0)
-        step.run(dev_in["h"], inp.W1, inp.b1, inp.W2, inp.lm_head, dev_in["X"], dev_in["q"], dev_in["k_new"],
-                 dev_in["v_new"], kc, vc, kl, tau, wl.posterior_threshold, wl.posterior_alpha)
-        for o, ho in zip(outs, host_out):
-            ho.copy_(o, non_blocking=True)
+    def upload(buf):
+        cs.wait_event(consumed[buf])          # the step that last read this buffer is done
+        with torch.cuda.stream(cs):
+            for k, v in host_in.items():
+                dev_bufs[buf][k].copy_(v, non_blocking=True)
+            root_bufs[buf].copy_(host_root, non_blocking=True)
+            copied[buf].record(cs)
 
-    with torch.cuda.stream(s):
-        for _ in range(3):
-            e2e_step()
+    def e2e_run(n, start_event=None):
+        with torch.cuda.stream(s):
+            for ev in consumed:
+                ev.record(s)
+        if start_event is not None:
+            cs.wait_event(start_event)
+        upload(0)
+        for i in range(n):
+            buf = i & 1
+            if i + 1 < n:
+                upload(buf ^ 1)
+            s.wait_event(copied[buf])
+            with torch.cuda.stream(s):
+                d = dev_bufs[buf]
+                step.root.copy_(root_bufs[buf])
+                kl.copy_(kv_len0)
+                step.run(d["h"], inp.W1, inp.b1, inp.W2, inp.lm_head, d["X"], d["q"], d["k_new"], d["v_new"], kc,
+                         vc, kl, tau, wl.posterior_threshold, wl.posterior_alpha)
+                consumed[buf].record(s)
+                for o, ho in zip(outs, host_out):
+                    ho.copy_(o, non_blocking=True)
+
+    e2e_run(3)
     torch.cuda.synchronize()
     if ws > 1:
         dist.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(s):
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record()
-        for _ in range(e2e_steps):
-            e2e_step()
-        e1.record()
+        e0.record(s)
+    e2e_run(e2e_steps, start_event=e0)
+    with torch.cuda.stream(s):
+        e1.record(s)
     torch.cuda.synchronize()
     te = torch.tensor([e0.elapsed_time(e1)], device=dev)
     if ws > 1:
@@ -320,16 +351,16 @@ def run_ours(args, ws, rank, local):
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": ws, "steps": args.steps,
         "warmup": max(3, args.warmup), "ms_per_step": round(ms_step, 5), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic (seeded, random-init weights)",
-        "config": {"workload": wl.name, "batch": wl.B, "hidden": wl.H, "vocab": wl.V, "heads": wl.K,
-                   "tree_nodes": T, "q_heads": wl.Hq, "kv_heads": wl.Hkv, "head_dim": wl.D, "kv_len": wl.L,
-                   "temperature": tau, "inputs": "planted accept path", "parallelism": f"replicas x{ws}",
-                   "l2": "per-step working set %.2f GB > 126 MB L2; no flush" % (total_bytes / 1e9),
-                   "timing": f"CUDA graphs of {S} steps, CUDA events; stage times from a separate replay with events between stages"},
+        "config": dict(workload_config(wl, T, tau, ws),
+                       l2="per-step working set %.2f GB > 126 MB L2; no flush" % (total_bytes / 1e9),
+                       timing=f"CUDA graphs of {S} steps, CUDA events; stage times from a separate replay with "
+                              "events between stages"),
         "roofline": roof,
         "step_roofline": {"bytes": total_bytes, "frac_hbm": round(total_bytes / (ms_step / 1e3) / 1e9 / hbm, 4)},
         "stages": stages,
         "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "note": "eager calls through MedusaStep.run with pinned host inputs/outputs"},
+                "note": "eager calls through MedusaStep.run; every step's inputs copied in from pinned host "
+                        "memory (next step's upload overlapped on a copy stream) and its results copied out"},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks,
         "dev_status": status,
@@ -385,7 +416,8 @@ def run_reference(args, ws, rank):
     return {"impl": "reference", "metric": METRIC, "value": cb["value"], "unit": UNIT, "n_gpus": ws,
             "steps": n, "warmup": 0, "ms_per_step": round(per * 1e3, 3), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
-            "config": {"workload": wl.name, "batch": wl.B, "temperature": args.temperature},
+            "config": dict(workload_config(wl, len(inp.choices) + 1, args.temperature, ws),
+                           timing="host wall clock (perf_counter) per oracle step"),
             "cpu_baseline": cb,
             "e2e": {"value": cb["value"], "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
