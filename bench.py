@@ -270,7 +270,7 @@ def run_ours(args, ws, rank, local):
     host_root = pin(root)
     dev_bufs = [{k: torch.empty_like(getattr(inp, k)) for k in host_in} for _ in range(2)]
     root_bufs = [torch.empty_like(root) for _ in range(2)]
-    outs = (step.accept_len, step.accepted_tokens, step.next_root, step.best_node)
+    outs = (step.results,)   # accept_len, best_path, best_node, next_root, accepted_tokens: one buffer
     host_out = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs]
     h2d = sum(v.numel() * v.element_size() for v in host_in.values()) + host_root.numel() * 4
     d2h = sum(o.numel() * o.element_size() for o in outs)
@@ -301,10 +301,9 @@ def run_ours(args, ws, rank, local):
             s.wait_event(copied[buf])
             with torch.cuda.stream(s):
                 d = dev_bufs[buf]
-                step.root.copy_(root_bufs[buf])
                 kl.copy_(kv_len0)
                 step.run(d["h"], inp.W1, inp.b1, inp.W2, inp.lm_head, d["X"], d["q"], d["k_new"], d["v_new"], kc,
-                         vc, kl, tau, wl.posterior_threshold, wl.posterior_alpha)
+                         vc, kl, tau, wl.posterior_threshold, wl.posterior_alpha, root=root_bufs[buf])
                 consumed[buf].record(s)
                 for o, ho in zip(outs, host_out):
                     ho.copy_(o, non_blocking=True)

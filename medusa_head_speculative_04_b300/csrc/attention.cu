@@ -1137,7 +1137,7 @@ int launch_attn_bf16(const medusa_tree* tree, const void* q, const void* k_new, 
       return MEDUSA_ERR_CUDA;
     const size_t smem = 1024 + TcLayout<D>::BYTES;
     auto k = tree_attn_tc_kernel<D>;
-    if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) != cudaSuccess)
+    if (!ensure_dyn_smem(k, smem))
       return MEDUSA_ERR_CUDA;
     if (launch_pdl(k, dim3(p.nctas), dim3(kTcThreads), smem, st, kc, vc, kt, vt, tq, a) != cudaSuccess) {
       (void)cudaGetLastError();
@@ -1146,7 +1146,7 @@ int launch_attn_bf16(const medusa_tree* tree, const void* q, const void* k_new, 
   } else {
     const size_t smem = 1024 + static_cast<size_t>(kStages) * 2 * (D / 64) * 8192 + 2 * kStages * 8;
     auto k = tree_attn_kernel<D>;
-    if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) != cudaSuccess)
+    if (!ensure_dyn_smem(k, smem))
       return MEDUSA_ERR_CUDA;
     if (launch_pdl(k, dim3(p.nctas), dim3((p.W + 1) * 32), smem, st, kc, vc, kt, vt, a) != cudaSuccess) {
       (void)cudaGetLastError();
@@ -1184,8 +1184,7 @@ MEDUSA_API int medusa_tree_attention(const medusa_tree* tree, const void* q, con
   if (dtype == MEDUSA_F32) {
     const size_t smem = static_cast<size_t>(Lmax + T) * 4;
     if (smem > 200 * 1024) return MEDUSA_ERR_UNSUPPORTED;
-    if (cudaFuncSetAttribute(tree_attn_f32_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem)) != cudaSuccess)
+    if (!ensure_dyn_smem(tree_attn_f32_kernel, smem))
       return MEDUSA_ERR_CUDA;
     if (launch_pdl(tree_attn_f32_kernel, dim3(B * T * Hq), dim3(128), smem, st, tree->dev,
                    static_cast<const float*>(q), static_cast<const float*>(k_new), static_cast<const float*>(v_new),

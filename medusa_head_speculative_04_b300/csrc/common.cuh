@@ -6,6 +6,9 @@
 #include <stdint.h>
 
 #include <cfloat>
+#include <map>
+#include <mutex>
+#include <utility>
 
 #include "../../include/medusa.h"
 
@@ -105,6 +108,28 @@ constexpr uint64_t kSpinLimitNs = 1000000000ull;
 
 // Process-wide count of kernels this library has launched (or captured).
 void note_launch();
+
+// Opt `kernel` in to `bytes` of dynamic shared memory.  The attribute stays
+// set, so the driver call is made only when a kernel needs more than it was
+// last given on the current device (per-step calls stay cheap on the host).
+template <typename... KArgs>
+bool ensure_dyn_smem(void (*kernel)(KArgs...), size_t bytes) {
+  static std::mutex mu;
+  static std::map<std::pair<const void*, int>, size_t> granted;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  const auto key = std::make_pair(reinterpret_cast<const void*>(kernel), dev);
+  std::lock_guard<std::mutex> lock(mu);
+  auto it = granted.find(key);
+  if (it != granted.end() && it->second >= bytes) return true;
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes)) !=
+      cudaSuccess) {
+    (void)cudaGetLastError();
+    return false;
+  }
+  granted[key] = bytes;
+  return true;
+}
 
 // Launch `kernel` with programmatic dependent launch allowed: the grid may
 // start while the previous kernel in the stream is still finishing, and the

@@ -289,7 +289,7 @@ int launch_heads(const HeadsPlan& p, const HeadsWs& w, const T* h, const T* W1, 
                  int32_t* topk_ids, float* topk_vals, int32_t* root_tok, cudaStream_t st) {
   const size_t xbytes = align_up(static_cast<size_t>(nb) * H * sizeof(T), 16);
   auto fc = heads_fc_kernel<T, BMAX>;
-  if (cudaFuncSetAttribute(fc, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(xbytes)) != cudaSuccess)
+  if (!ensure_dyn_smem(fc, xbytes))
     return MEDUSA_ERR_CUDA;
   if (launch_pdl(fc, dim3(p.fc_ctas), dim3(kThreads), xbytes, st, h + static_cast<size_t>(b0) * H, W1, b1, H, K, nb,
                  static_cast<T*>(w.u) + static_cast<size_t>(b0) * K * H) != cudaSuccess) {
@@ -299,7 +299,7 @@ int launch_heads(const HeadsPlan& p, const HeadsWs& w, const T* h, const T* W1, 
   MEDUSA_LAUNCH_CHECK();
   const size_t smem = vocab_smem_bytes(nb, BMAX, H, sizeof(T), p.rpc, p.cph, topk);
   auto vk = heads_vocab_kernel<T, BMAX>;
-  if (cudaFuncSetAttribute(vk, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) != cudaSuccess)
+  if (!ensure_dyn_smem(vk, smem))
     return MEDUSA_ERR_CUDA;
   if (launch_pdl(vk, dim3(p.nblk * p.cph), dim3(kThreads), smem, st, h, static_cast<const T*>(w.u), W2, lm, B, b0, nb,
                  H, V, K, topk, p.rpc, p.cph, head_logits, topk_ids, topk_vals, root_tok, w.cand_v, w.cand_i,

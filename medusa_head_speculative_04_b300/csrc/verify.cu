@@ -707,7 +707,7 @@ int launch_tc(const VerifyPlan& p, const CUtensorMap& mx, const CUtensorMap& mw,
   if (sh.sw < 2) return MEDUSA_ERR_UNSUPPORTED;
   const size_t smem = tc_smem_bytes(sh);
   auto k = verify_tc_kernel<BN>;
-  if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) != cudaSuccess)
+  if (!ensure_dyn_smem(k, smem))
     return MEDUSA_ERR_CUDA;
   if (launch_pdl(k, dim3(p.n_mt * p.n_nt), dim3(kTcThreads), smem, st, mx, mw, H, p.n_mt, sh, ea) != cudaSuccess) {
     (void)cudaGetLastError();
@@ -783,7 +783,7 @@ MEDUSA_API int medusa_verify_accept(const medusa_tree* tree, const void* x, cons
       const size_t smem = static_cast<size_t>(nb) * H * 4;
       if (smem > 200 * 1024) return MEDUSA_ERR_UNSUPPORTED;
       auto k = nb <= 4 ? verify_gemv_f32_kernel<4> : nb <= 8 ? verify_gemv_f32_kernel<8> : verify_gemv_f32_kernel<16>;
-      if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) != cudaSuccess)
+      if (!ensure_dyn_smem(k, smem))
         return MEDUSA_ERR_CUDA;
       if (launch_pdl(k, dim3(ctas), dim3(kThreads), smem, st, static_cast<const float*>(x),
                      static_cast<const float*>(lm_head), r0, nb, H, V, groups, z) != cudaSuccess) {

@@ -38,11 +38,15 @@ class MedusaStep:
         self.positions = torch.zeros(B, T, **i32)
         self.candidates = torch.zeros(B, P, W, **i32)
         self.attn_out = torch.zeros(B, T, Hq, D, **f32)
-        self.accept_len = torch.zeros(B, **i32)
-        self.best_path = torch.zeros(B, **i32)
-        self.best_node = torch.zeros(B, **i32)
-        self.accepted_tokens = torch.zeros(B, W, **i32)
-        self.next_root = torch.zeros(B, **i32)
+        # the per-request results share one buffer, so a caller can read them with one copy;
+        # each part starts on a 16-byte boundary, as the C entry points require
+        Bp = (B + 3) // 4 * 4
+        self.results = torch.zeros(4 * Bp + B * W, **i32)
+        self.accept_len = self.results[0:B]
+        self.best_path = self.results[Bp:Bp + B]
+        self.best_node = self.results[2 * Bp:2 * Bp + B]
+        self.next_root = self.results[3 * Bp:3 * Bp + B]
+        self.accepted_tokens = self.results[4 * Bp:].view(B, W)
         self.dev_status = torch.zeros(B, **i32)
         self.head_logits = torch.zeros(B, K, V, **f32) if keep_head_logits else None
         self.logits = torch.zeros(B, T, V, **f32) if keep_logits else None
@@ -63,9 +67,9 @@ class MedusaStep:
                              self.topk_ids, self.topk_vals, self.root, self.ws_heads,
                              head_logits=self.head_logits, stream=stream)
 
-    def build(self, kv_len, stream=None):
-        mb.medusa_build_tree(self.tree, self.root, self.topk_ids, kv_len, self.tokens, self.positions,
-                             self.candidates, self.dev_status, stream=stream)
+    def build(self, kv_len, root=None, stream=None):
+        mb.medusa_build_tree(self.tree, self.root if root is None else root, self.topk_ids, kv_len, self.tokens,
+                             self.positions, self.candidates, self.dev_status, stream=stream)
 
     def attention(self, q, k_new, v_new, k_cache, v_cache, kv_len, stream=None):
         mb.medusa_tree_attention(self.tree, q, k_new, v_new, k_cache, v_cache, kv_len, self.attn_out,
@@ -85,7 +89,7 @@ class MedusaStep:
     def run(self, h, W1, b1, W2, lm_head, X, q, k_new, v_new, k_cache, v_cache, kv_len, temperature: float,
             threshold: float = 0.09, alpha: float = 0.3, root: Optional[torch.Tensor] = None, stream=None):
         """One whole step.  ``root`` (int32 [B], device) is the previous step's next token; it is
-        ignored when the step derives the root from lm_head(h)."""
+        copied into ``self.root`` and ignored when the step derives the root from lm_head(h)."""
         if root is not None and not self.root_from_lm_head:
             self.root.copy_(root)
         self.heads(h, W1, b1, W2, lm_head, stream=stream)
