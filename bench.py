@@ -47,7 +47,30 @@ def parse_args():
     ap.add_argument("--unroll", type=int, default=20, help="steps per captured CUDA graph")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget-s", type=float, default=30.0)
+    ap.add_argument("--tree", default=None,
+                    help="replace the workload's tree: 'cartesian:k1,k2,...' (full product tree) or "
+                         "'seeded:N[:f0,f1,...]' (seeded sparse tree of N nodes, per-depth fan-out bounds)")
     return ap.parse_args()
+
+
+def select_workload(args):
+    """The named workload, with its candidate tree replaced when --tree is given."""
+    import dataclasses
+    import synth
+    wl = synth.WORKLOADS[args.workload]
+    if not args.tree:
+        return wl
+    kind, _, rest = args.tree.partition(":")
+    if kind == "cartesian":
+        tree = ("cartesian", tuple(int(x) for x in rest.split(",")))
+    elif kind == "seeded":
+        n, _, fan = rest.partition(":")
+        tree = ("seeded", int(n), tuple(int(x) for x in fan.split(",")) if fan else synth.TREE64[2])
+    else:
+        raise SystemExit(f"--tree: unknown kind {kind!r}")
+    if kind == "cartesian" and len(tree[1]) > wl.K:
+        raise SystemExit("--tree: deeper than the workload's number of heads")
+    return dataclasses.replace(wl, name=f"{wl.name}/tree={args.tree}", tree=tree)
 
 
 def dist_env():
@@ -148,7 +171,7 @@ def measured_peaks():
 
 def workload_config(wl, T, tau, ws):
     """The workload keys both arms report."""
-    return {"workload": wl.name, "batch": wl.B, "hidden": wl.H, "vocab": wl.V, "heads": wl.K, "tree_nodes": T,
+    return {"workload": wl.name, "tree": "%s %s" % (wl.tree[0], wl.tree[1:]), "batch": wl.B, "hidden": wl.H, "vocab": wl.V, "heads": wl.K, "tree_nodes": T,
             "q_heads": wl.Hq, "kv_heads": wl.Hkv, "head_dim": wl.D, "kv_len": wl.L, "temperature": tau,
             "inputs": "planted accept path", "parallelism": f"replicas x{ws}"}
 
@@ -164,7 +187,7 @@ def run_ours(args, ws, rank, local):
 
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    wl = synth.WORKLOADS[args.workload]
+    wl = select_workload(args)
     inp = synth.make_inputs(wl, dev, variant="plant")
     T = inp.T
     step = mb.MedusaStep(inp.choices, wl.B, wl.H, wl.V, wl.K, wl.Hq, wl.Hkv, wl.D, wl.Lmax, wl.k_needed(),
@@ -268,8 +291,8 @@ def run_ours(args, ws, rank, local):
     pin = lambda x: x.detach().cpu().pin_memory()
     host_in = {k: pin(getattr(inp, k)) for k in ("h", "X", "q", "k_new", "v_new")}
     host_root = pin(root)
-    dev_bufs = [{k: torch.empty_like(getattr(inp, k)) for k in host_in} for _ in range(2)]
-    root_bufs = [torch.empty_like(root) for _ in range(2)]
+    dev_bufs = [{k: getattr(inp, k).clone() for k in host_in} for _ in range(2)]
+    root_bufs = [root.clone() for _ in range(2)]
     outs = (step.results,)   # accept_len, best_path, best_node, next_root, accepted_tokens: one buffer
     host_out = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs]
     h2d = sum(v.numel() * v.element_size() for v in host_in.values()) + host_root.numel() * 4
@@ -287,7 +310,19 @@ def run_ours(args, ws, rank, local):
             root_bufs[buf].copy_(host_root, non_blocking=True)
             copied[buf].record(cs)
 
-    def e2e_run(n, start_event=None):
+    def run_step(buf):
+        d = dev_bufs[buf]
+        kl.copy_(kv_len0)
+        step.run(d["h"], inp.W1, inp.b1, inp.W2, inp.lm_head, d["X"], d["q"], d["k_new"], d["v_new"], kc,
+                 vc, kl, tau, wl.posterior_threshold, wl.posterior_alpha, root=root_bufs[buf])
+
+    # the serving form of the call: one CUDA graph of MedusaStep.run per input buffer
+    step_graphs = [step.capture(dev_bufs[b]["h"], inp.W1, inp.b1, inp.W2, inp.lm_head, dev_bufs[b]["X"],
+                                dev_bufs[b]["q"], dev_bufs[b]["k_new"], dev_bufs[b]["v_new"], kc, vc, kl, tau,
+                                wl.posterior_threshold, wl.posterior_alpha, root=root_bufs[b],
+                                prologue=lambda: kl.copy_(kv_len0), stream=s) for b in range(2)]
+
+    def e2e_run(n, graphs, start_event=None):
         with torch.cuda.stream(s):
             for ev in consumed:
                 ev.record(s)
@@ -300,29 +335,33 @@ def run_ours(args, ws, rank, local):
                 upload(buf ^ 1)
             s.wait_event(copied[buf])
             with torch.cuda.stream(s):
-                d = dev_bufs[buf]
-                kl.copy_(kv_len0)
-                step.run(d["h"], inp.W1, inp.b1, inp.W2, inp.lm_head, d["X"], d["q"], d["k_new"], d["v_new"], kc,
-                         vc, kl, tau, wl.posterior_threshold, wl.posterior_alpha, root=root_bufs[buf])
+                if graphs:
+                    step_graphs[buf].replay()
+                else:
+                    run_step(buf)
                 consumed[buf].record(s)
                 for o, ho in zip(outs, host_out):
                     ho.copy_(o, non_blocking=True)
 
-    e2e_run(3)
-    torch.cuda.synchronize()
-    if ws > 1:
-        dist.barrier()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(s):
-        e0.record(s)
-    e2e_run(e2e_steps, start_event=e0)
-    with torch.cuda.stream(s):
-        e1.record(s)
-    torch.cuda.synchronize()
-    te = torch.tensor([e0.elapsed_time(e1)], device=dev)
-    if ws > 1:
-        dist.all_reduce(te, op=dist.ReduceOp.MAX)
-    e2e_value = e2e_steps * wl.B * ws / (float(te.item()) / 1e3)
+    def e2e_time(graphs):
+        e2e_run(3, graphs)
+        torch.cuda.synchronize()
+        if ws > 1:
+            dist.barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(s):
+            e0.record(s)
+        e2e_run(e2e_steps, graphs, start_event=e0)
+        with torch.cuda.stream(s):
+            e1.record(s)
+        torch.cuda.synchronize()
+        te = torch.tensor([e0.elapsed_time(e1)], device=dev)
+        if ws > 1:
+            dist.all_reduce(te, op=dist.ReduceOp.MAX)
+        return e2e_steps * wl.B * ws / (float(te.item()) / 1e3)
+
+    e2e_value = e2e_time(graphs=True)
+    e2e_eager = e2e_time(graphs=False)
 
     if rank != 0:
         return None
@@ -337,7 +376,7 @@ def run_ours(args, ws, rank, local):
         roof = {"kernel": "medusa_heads_topk (heads_fc + heads_vocab_topk)", "bound": "hbm",
                 "achieved": round(ach, 1), "peak": hbm, "unit": "GB/s", "frac": round(ach / hbm, 4),
                 "peak_source": src, "algorithmic_bytes": sb["heads"],
-                "traffic": traffic_from_profile("heads_vicuna7b")}
+                "traffic": traffic_from_profile("heads_vicuna7b") if wl.name == "vicuna7b" else None}
     stages = {}
     for k, v in stage_ms.items():
         if v:
@@ -358,8 +397,11 @@ def run_ours(args, ws, rank, local):
         "step_roofline": {"bytes": total_bytes, "frac_hbm": round(total_bytes / (ms_step / 1e3) / 1e9 / hbm, 4)},
         "stages": stages,
         "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "note": "eager calls through MedusaStep.run; every step's inputs copied in from pinned host "
-                        "memory (next step's upload overlapped on a copy stream) and its results copied out"},
+                "eager_value": round(e2e_eager, 2),
+                "note": "MedusaStep.run captured once per input buffer (MedusaStep.capture) and replayed; every "
+                        "step's inputs copied in from pinned host memory (the next step's upload overlapped on a "
+                        "copy stream) and its results copied out; eager_value: the same loop with eager "
+                        "MedusaStep.run calls"},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks,
         "dev_status": status,
@@ -406,7 +448,7 @@ def run_reference(args, ws, rank):
         return None
     import torch
     import synth
-    wl = synth.WORKLOADS[args.workload]
+    wl = select_workload(args)
     # inputs come from the seeded generator (on a GPU when there is one, as it is much
     # faster there); the oracle only ever sees host copies
     gen_dev = "cuda" if torch.cuda.is_available() else "cpu"

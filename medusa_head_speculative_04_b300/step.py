@@ -97,3 +97,28 @@ class MedusaStep:
         self.attention(q, k_new, v_new, k_cache, v_cache, kv_len, stream=stream)
         self.verify(X, lm_head, temperature, threshold, alpha, stream=stream)
         self.commit(k_new, v_new, k_cache, v_cache, kv_len, stream=stream)
+
+    def capture(self, *args, prologue=None, stream: Optional[torch.cuda.Stream] = None, **kwargs):
+        """Capture one whole step (the arguments of :meth:`run`) in a CUDA graph.
+
+        The graph keeps the tensors it was captured with: refill them in place and
+        ``replay()`` it to run the next step with one launch from the host.
+        ``prologue`` (a callable, or None) is captured just before the step, on the
+        same stream.  One eager step runs first, so its outputs change state
+        (``kv_len`` and the cache rows it commits) like any other step.
+        """
+        cur = torch.cuda.current_stream(self.device)
+        s = stream if stream is not None else torch.cuda.Stream(self.device)  # capture needs a side stream
+        s.wait_stream(cur)
+        with torch.cuda.stream(s):
+            if prologue is not None:
+                prologue()
+            self.run(*args, **kwargs)     # sets the kernels' attributes outside the capture
+        s.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            if prologue is not None:
+                prologue()
+            self.run(*args, **kwargs)
+        cur.wait_stream(s)
+        return g

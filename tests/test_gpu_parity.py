@@ -173,6 +173,32 @@ def test_small_bf16_full_step(mb, wl, temperature, variant):
     assert near <= 3
 
 
+def test_captured_step_replays_new_inputs(mb):
+    """MedusaStep.capture: a graph replay after the captured tensors are refilled in place
+    computes the step of the new contents (checked against the oracle)."""
+    wl = SMALL_BF16
+    inp = synth.make_inputs(wl, "cuda", variant="plant")
+    step = make_step(mb, wl, inp)
+    kc, vc, kl0 = inp.k_cache.clone(), inp.v_cache.clone(), inp.kv_len.clone()
+    kl = kl0.clone()
+    act = {k: getattr(inp, k).clone() for k in ("h", "X", "q", "k_new", "v_new", "root")}
+    g = step.capture(act["h"], inp.W1, inp.b1, inp.W2, inp.lm_head, act["X"], act["q"], act["k_new"],
+                     act["v_new"], kc, vc, kl, 0.7, wl.posterior_threshold, wl.posterior_alpha, root=act["root"],
+                     prologue=lambda: kl.copy_(kl0))
+    other = synth.make_inputs(dataclasses.replace(wl, config_id=14), "cuda", variant="random")
+    for k in act:
+        act[k].copy_(getattr(other, k))
+    kc.copy_(inp.k_cache)
+    vc.copy_(inp.v_cache)
+    for t in (step.results, step.attn_out, step.logits, step.head_logits, step.dev_status):
+        t.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    mixed = dataclasses.replace(inp, **{k: getattr(other, k) for k in act}, plant=None)
+    near = check_full(wl, mixed, step, kc, vc, kl, 0.7)
+    assert near <= 3
+
+
 def test_root_only_tree(mb):
     """Degenerate tree without candidates: only the root is emitted, accept_length 0."""
     wl = dataclasses.replace(synth.WORKLOADS["tiny"], name="root_only", tree=("cartesian", ()))
