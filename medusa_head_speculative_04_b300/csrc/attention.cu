@@ -91,15 +91,6 @@ AttnWs carve_attn_ws(void* base, const AttnPlan& p, int D) {
   return w;
 }
 
-int sm_count() {
-  int dev = 0, n = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
-    (void)cudaGetLastError();
-    return 148;
-  }
-  return n;
-}
-
 constexpr int kMaxVisTiles = 128;  // query tiles whose tree visibility travels in the launch arguments
 
 struct AttnArgs {
@@ -530,12 +521,6 @@ struct TcLayout {
   __device__ static uint32_t p_off(int st, int ti) { return P_IN_K ? OFF_KV + st * STAGE : OFF_P + (ti & 1) * P_BYTES; }
 };
 
-// 2^x on the special-function unit (flush-to-zero; 2^-inf = 0).
-__device__ inline float ex2_approx(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
 
 // Visible tiles of a segment (cache tiles always, tree tiles per the mask).
 __device__ inline int seg_visible_tiles(const Seg& sg, uint64_t vis) {
@@ -1089,7 +1074,7 @@ MEDUSA_API size_t medusa_tree_attention_workspace_size(const medusa_tree* tree, 
                                                        medusa_dtype dtype) {
   if (!tree || B < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv || Lmax < 0) return 0;
   if (dtype == MEDUSA_F32) return 256;
-  AttnPlan p = plan_attn(tree->T, B, Hq, Hkv, Lmax, kv_len_hint, sm_count());
+  AttnPlan p = plan_attn(tree->T, B, Hq, Hkv, Lmax, kv_len_hint, device_sm_count());
   return carve_attn_ws(nullptr, p, D).bytes;
 }
 
@@ -1196,7 +1181,7 @@ MEDUSA_API int medusa_tree_attention(const medusa_tree* tree, const void* q, con
     MEDUSA_LAUNCH_CHECK();
     return MEDUSA_OK;
   }
-  AttnPlan p = plan_attn(T, B, Hq, Hkv, Lmax, kv_len_hint, sm_count());
+  AttnPlan p = plan_attn(T, B, Hq, Hkv, Lmax, kv_len_hint, device_sm_count());
   AttnWs w = carve_attn_ws(ws, p, D);
   if (!ws || ws_bytes < w.bytes) return MEDUSA_ERR_WORKSPACE;
   if (D == 128)

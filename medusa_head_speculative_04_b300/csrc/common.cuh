@@ -103,11 +103,21 @@ __device__ inline uint64_t globaltimer_ns() {
 __device__ inline void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ inline void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
+// 2^x on the special-function unit (flush-to-zero; 2^-inf = 0).
+__device__ inline float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // Bounded-wait limit for every device-side spin (about one second).
 constexpr uint64_t kSpinLimitNs = 1000000000ull;
 
 // Process-wide count of kernels this library has launched (or captured).
 void note_launch();
+
+// Streaming multiprocessors of the current device (148 when the query fails).
+int device_sm_count();
 
 // Opt `kernel` in to `bytes` of dynamic shared memory.  The attribute stays
 // set, so the driver call is made only when a kernel needs more than it was

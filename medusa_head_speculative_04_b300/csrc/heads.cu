@@ -48,15 +48,6 @@ struct HeadsPlan {
   int fc_ctas;
 };
 
-int device_sms() {
-  int dev = 0, n = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
-    (void)cudaGetLastError();
-    return 148;
-  }
-  return n;
-}
-
 constexpr size_t kSmemTwoPerSm = 110 * 1024;   // two CTAs per SM fit below this
 constexpr size_t kSmemMax = 220 * 1024;        // per-CTA dynamic shared memory used at most
 
@@ -78,7 +69,7 @@ int bmax_of(int nb) { return nb == 1 ? 1 : nb == 2 ? 2 : nb <= 4 ? 4 : nb <= 8 ?
 // Returns false when no split fits in shared memory.
 bool plan_heads(int B, int H, int V, int K, int with_root, int esize, int topk, HeadsPlan* out) {
   HeadsPlan p{};
-  const int sms = device_sms();
+  const int sms = device_sm_count();
   p.nblk = K + (with_root ? 1 : 0);
   p.bgroup = static_cast<int>(std::min<size_t>(16, std::max<size_t>(1, kMaxXBytes / (static_cast<size_t>(H) * esize))));
   p.bgroup = std::min(p.bgroup, B);

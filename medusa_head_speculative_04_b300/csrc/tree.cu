@@ -19,6 +19,15 @@ using namespace medusa;
 namespace medusa {
 static std::atomic<uint64_t> g_launches{0};
 void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
+int device_sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return 148;
+  }
+  return n;
+}
 }  // namespace medusa
 
 MEDUSA_API uint64_t medusa_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
@@ -96,12 +105,16 @@ MEDUSA_API int medusa_tree_create(const int32_t* ranks_flat, const int32_t* lens
   t->P = static_cast<int32_t>(t->leaf.size());
   const int W = t->dmax + 1;
   t->paths.assign(static_cast<size_t>(t->P) * W, -1);
+  t->first_path.assign(T, -1);
   for (int p = 0; p < t->P; ++p) {
-    for (int a = t->leaf[p]; a >= 0; a = t->parent[a]) t->paths[static_cast<size_t>(p) * W + t->depth[a]] = a;
+    for (int a = t->leaf[p]; a >= 0; a = t->parent[a]) {
+      t->paths[static_cast<size_t>(p) * W + t->depth[a]] = a;
+      if (t->first_path[a] < 0) t->first_path[a] = p;
+    }
   }
 
   // one device block holding every table
-  const size_t n_i32 = 5 * static_cast<size_t>(T) + t->paths.size() + t->leaf.size();
+  const size_t n_i32 = 6 * static_cast<size_t>(T) + t->paths.size() + t->leaf.size();
   const size_t bytes_i32 = align_up(n_i32 * 4, 256);
   const size_t bytes = bytes_i32 + t->mask.size() * 4;
   cudaGetDevice(&t->device);
@@ -111,6 +124,7 @@ MEDUSA_API int medusa_tree_create(const int32_t* ranks_flat, const int32_t* lens
   auto put = [&](const std::vector<int32_t>& v) { size_t s = o; std::copy(v.begin(), v.end(), host.begin() + o); o += v.size(); return s; };
   size_t o_parent = put(t->parent), o_depth = put(t->depth), o_rank = put(t->rank);
   size_t o_cs = put(t->child_start), o_cc = put(t->child_count), o_paths = put(t->paths), o_leaf = put(t->leaf);
+  size_t o_fp = put(t->first_path);
   auto* base = static_cast<int32_t*>(t->dev_block);
   auto* mask = reinterpret_cast<uint32_t*>(static_cast<char*>(t->dev_block) + bytes_i32);
   if (cudaMemcpy(base, host.data(), n_i32 * 4, cudaMemcpyHostToDevice) != cudaSuccess ||
@@ -120,7 +134,7 @@ MEDUSA_API int medusa_tree_create(const int32_t* ranks_flat, const int32_t* lens
     return MEDUSA_ERR_CUDA;
   }
   t->dev = medusa_tree_dev{T, t->P, t->dmax, t->mask_words, base + o_parent, base + o_depth, base + o_rank,
-                           base + o_cs, base + o_cc, mask, base + o_paths, base + o_leaf};
+                           base + o_cs, base + o_cc, mask, base + o_paths, base + o_leaf, base + o_fp};
   *out = t;
   return MEDUSA_OK;
 }

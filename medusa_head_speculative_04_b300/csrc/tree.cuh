@@ -20,13 +20,14 @@ struct medusa_tree_dev {
   const uint32_t* mask;        // [T * mask_words] ancestor-or-self bits
   const int32_t* paths;        // [P * (dmax+1)]
   const int32_t* leaf;         // [P]
+  const int32_t* first_path;   // [T] lowest path index whose leaf descends from (or is) the node
 };
 
 struct medusa_tree {
   int32_t T = 0, P = 0, dmax = 0, mask_words = 0;
   int32_t max_rank[MEDUSA_MAX_DEPTH] = {};
   int device = 0;
-  std::vector<int32_t> parent, depth, rank, child_start, child_count, paths, leaf;
+  std::vector<int32_t> parent, depth, rank, child_start, child_count, paths, leaf, first_path;
   std::vector<uint32_t> mask;
   void* dev_block = nullptr;
   medusa_tree_dev dev{};

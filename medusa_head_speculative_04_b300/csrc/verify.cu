@@ -80,30 +80,55 @@ constexpr int F32_TILE = 256;  // vocabulary columns per statistics tile on the 
 
 struct VerifyPlan {
   int R, BN, n_mt, n_nt;
+  int qr, n_tiles, grid;  // bf16: rows per TMEM lane quadrant, tiles, persistent CTAs
+  int n_parts;            // statistics partials per row (bf16, one row tile: one per CTA)
 };
 
+// bf16: the row tiles split the B*T rows evenly (4*qr <= 128 rows each).  With
+// one row tile the GEMM streams lm_head once: BN minimises what the busiest
+// CTA loads, its lm_head rows plus the tree rows X again for every tile (X
+// rows cost about twice a weight row: every CTA requests the same lines), and
+// a little for the last tile's exposed epilogue.  At the 7B vocabulary that
+// is one 224-column tile per CTA.  With several row tiles the GEMM is
+// compute-bound and takes the widest MMA.
 VerifyPlan plan_verify(int B, int T, int V, medusa_dtype dt) {
   VerifyPlan p{};
   p.R = B * T;
   if (dt == MEDUSA_BF16) {
+    const int sms = device_sm_count();
     p.n_mt = cdiv(p.R, BM);
-    if (p.n_mt == 1)
-      p.BN = std::min(256, std::max(16, cdiv(cdiv(V, 148), 16) * 16));
-    else
+    p.qr = cdiv(p.R, 4 * p.n_mt);
+    if (p.n_mt == 1) {
+      long best = -1;
+      for (int bn = 16; bn <= 256; bn += 16) {
+        const long per_cta = cdiv(cdiv(V, bn), sms);
+        const long cost = 8 * per_cta * (bn + 8 * p.qr) + bn;
+        if (best < 0 || cost <= best) {
+          best = cost;
+          p.BN = bn;
+        }
+      }
+    } else {
       p.BN = 256;
+    }
     p.n_nt = cdiv(V, p.BN);
+    p.n_tiles = p.n_mt * p.n_nt;
+    p.grid = std::min(p.n_tiles, sms);
+    p.n_parts = p.n_mt == 1 ? p.grid : p.n_nt;
   } else {
     p.n_mt = 1;
     p.BN = F32_TILE;
     p.n_nt = cdiv(V, F32_TILE);
+    p.n_parts = p.n_nt;
   }
   return p;
 }
 
 struct VerifyWs {
-  float4* part;      // [R, n_nt] (max, sum exp, sum exp*y, argmax bits)
+  float4* part;      // [R, n_parts] (max, sum exp, sum exp*y, argmax bits)
   float* child_z;    // [R] logit of node c's token under its parent (indexed by c)
   float4* rowst;     // [R] merged statistics
+  unsigned char* acc;  // [R] each node's acceptance test against its parent
   int* tickets;      // [B] CTAs done with a request's nodes (self-resetting)
   float* zbuf;       // fp32 path: [R, V] logits when the caller gives none
   size_t bytes;
@@ -113,8 +138,9 @@ VerifyWs carve_verify_ws(void* base, const VerifyPlan& p, int V, medusa_dtype dt
   VerifyWs w{};
   size_t o = 0;
   auto take = [&](size_t n) { size_t s = o; o = align_up(o + n, 256); return s; };
-  size_t op = take(static_cast<size_t>(p.R) * p.n_nt * 16), oc = take(static_cast<size_t>(p.R) * 4),
-         orow = take(static_cast<size_t>(p.R) * 16), otk = take(static_cast<size_t>(p.R) * 4);
+  size_t op = take(static_cast<size_t>(p.R) * p.n_parts * 16), oc = take(static_cast<size_t>(p.R) * 4),
+         orow = take(static_cast<size_t>(p.R) * 16), otk = take(static_cast<size_t>(p.R) * 4),
+         oa = take(static_cast<size_t>(p.R));
   size_t oz = dt == MEDUSA_F32 ? take(static_cast<size_t>(p.R) * V * 4) : 0;
   char* c = static_cast<char*>(base);
   if (c) {
@@ -122,6 +148,7 @@ VerifyWs carve_verify_ws(void* base, const VerifyPlan& p, int V, medusa_dtype dt
     w.child_z = reinterpret_cast<float*>(c + oc);
     w.rowst = reinterpret_cast<float4*>(c + orow);
     w.tickets = reinterpret_cast<int*>(c + otk);
+    w.acc = reinterpret_cast<unsigned char*>(c + oa);
     w.zbuf = dt == MEDUSA_F32 ? reinterpret_cast<float*>(c + oz) : nullptr;
   }
   w.bytes = o;
@@ -140,80 +167,100 @@ struct EpiArgs {
 };
 
 // ------------------------------------------------------------------------
-// K5, bf16: tcgen05 GEMM with the statistics epilogue.
-// Warps 0..kEpiWarps-1 run the epilogue (warp w reads TMEM lanes 32*(w%4)..
-// and the (w/4)-th of kEpiWarps/4 column groups of the tile); the next warp
-// streams lm_head tiles, the next issues the MMAs and owns TMEM, the last
-// streams the tree rows X.
+// K5, bf16: persistent tcgen05 GEMM with the statistics epilogue.
+// A tile is 4*qr tree rows x BN vocabulary columns; CTA c takes tiles c,
+// c + grid, ...  Warps 0..kEpiWarps-1 run the epilogue (warp w reads TMEM
+// lanes 32*(w%4).. and the (w/4)-th of kEpiWarps/4 column groups); the next
+// warp streams lm_head tiles, the next issues the MMAs and owns TMEM, the last
+// streams the tree rows X.  Two TMEM accumulators alternate between tiles, so
+// the epilogue of one tile runs under the MMAs of the next.
+// A tile's rows are spread over the four TMEM lane quadrants (qr <= 32 rows
+// each: quadrant q of row tile m holds rows m*4*qr + q*qr ..), so that small
+// trees keep every epilogue warp busy; X stages are 128 rows (four TMA boxes
+// of qr rows at shared-memory rows 0, 32, 64, 96; rows past a box are never
+// written and feed only accumulator rows that are never read).
 // lm_head (from HBM) and X (from L2, shared by every CTA) run in separate
-// rings: a deep one for the weight stream, a shallow one for X, whose stage
-// holds only the xr rows the tile has (xr <= 128; the MMA's reads of rows
-// xr..127 land in the next stage's bytes and only feed accumulator rows that
-// are never read).
+// rings: a deep one for the weight stream, a shallow one for X.
 // ------------------------------------------------------------------------
-constexpr int kMaxStages = 8;
+constexpr int kMaxStagesW = 16;
+constexpr int kMaxStagesX = 4;
+constexpr uint32_t kXStageBytes = BM * BK * 2;
 constexpr int kEpiWarps = 8;
 constexpr int kWarpW = kEpiWarps, kWarpMma = kEpiWarps + 1, kWarpX = kEpiWarps + 2;
 constexpr int kTcThreads = (kEpiWarps + 3) * 32;
 constexpr int kColGroups = kEpiWarps / 4;
-constexpr size_t kHalfXchgBytes = (kColGroups - 1) * BM * 5 * 4;  // per-row statistics of groups 1..
-
+constexpr size_t kXchgBytes = 2 * (kColGroups - 1) * BM * 5 * 4;  // per-row statistics of groups 1.., 2 buffers
 
 struct TcShape {
-  int BN, xr, sw, sx;  // vocab tile, X rows per stage, lm_head stages, X stages
+  int BN;       // vocabulary columns per tile
+  int qr;       // tree rows per TMEM lane quadrant (a row tile holds 4*qr rows)
+  int n_mt;     // row tiles
+  int n_tiles;  // n_mt * vocabulary tiles; tile t is row tile t % n_mt, vocabulary tile t / n_mt
+  int sw;       // lm_head ring stages
+  int sx;       // X ring stages (<= kMaxStagesX)
 };
 
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
-// Running statistics of one row over a 32-column chunk v[0..nv): maximum and
-// its first column (tree reduction), then, at temperature > 0, the sums
-// s = sum 2^y2 and w2 = sum 2^y2 * y2 with y2 = (z - m) * k2, k2 = log2(e) /
-// temperature, rescaled when the maximum grows.  NaN never wins the maximum.
-__device__ inline void chunk_stats(const float (&v)[32], int nv, int col0, float k2, bool tempered, float& m,
+// Running statistics of one row over a block of NCH*16 columns v[0..nv):
+// maximum and its first column (tree reduction per 16 columns, then the
+// chunks in column order), then, at temperature > 0, the sums s = sum 2^y2
+// and w2 = sum 2^y2 * y2 with y2 = (z - m) * k2, k2 = log2(e) / temperature,
+// rescaled when the maximum grows.  NaN never wins the maximum.
+template <int NCH>
+__device__ inline void block_stats(float (&v)[NCH * 16], int nv, int col0, float k2, bool tempered, float& m,
                                    int& arg, float& s, float& w2, bool& nan_seen) {
-  float t[32];
+  constexpr int N = NCH * 16;
 #pragma unroll
-  for (int j = 0; j < 32; ++j) {
+  for (int j = 0; j < N; ++j) {
     const bool in = j < nv;
     nan_seen |= in && v[j] != v[j];
-    t[j] = (in && v[j] == v[j]) ? v[j] : -INFINITY;
+    v[j] = (in && v[j] == v[j]) ? v[j] : -INFINITY;
   }
-  float tv[16];
-  int ti[16];
+  float bm = -INFINITY;
+  int bi = 0;
 #pragma unroll
-  for (int j = 0; j < 16; ++j) {
-    const bool take = t[j + 16] > t[j];
-    tv[j] = take ? t[j + 16] : t[j];
-    ti[j] = take ? j + 16 : j;
-  }
+  for (int c = 0; c < NCH; ++c) {
+    float tv[8];
+    int ti[8];
 #pragma unroll
-  for (int h = 8; h >= 1; h >>= 1) {
+    for (int j = 0; j < 8; ++j) {
+      const bool take = v[c * 16 + j + 8] > v[c * 16 + j];
+      tv[j] = take ? v[c * 16 + j + 8] : v[c * 16 + j];
+      ti[j] = take ? j + 8 : j;
+    }
 #pragma unroll
-    for (int j = 0; j < h; ++j) {
-      const bool take = tv[j + h] > tv[j];
-      tv[j] = take ? tv[j + h] : tv[j];
-      ti[j] = take ? ti[j + h] : ti[j];
+    for (int h = 4; h >= 1; h >>= 1) {
+#pragma unroll
+      for (int j = 0; j < h; ++j) {
+        const bool take = tv[j + h] > tv[j];
+        tv[j] = take ? tv[j + h] : tv[j];
+        ti[j] = take ? ti[j + h] : ti[j];
+      }
+    }
+    if (tv[0] > bm) {
+      bm = tv[0];
+      bi = c * 16 + ti[0];
     }
   }
-  const float cm = tv[0];
-  if (cm > m) {
+  if (bm > m) {
     if (tempered && s > 0.f) {
-      const float d2 = (m - cm) * k2;
-      const float sc = exp2f(d2);
+      const float d2 = (m - bm) * k2;
+      const float sc = ex2_approx(d2);
       w2 = sc * fmaf(d2, s, w2);
       s *= sc;
     }
-    m = cm;
-    arg = col0 + ti[0];
+    m = bm;
+    arg = col0 + bi;
   }
   if (tempered && m != -INFINITY) {
     const float b2 = -m * k2;
     float s4[4] = {0.f, 0.f, 0.f, 0.f}, w4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int j = 0; j < 32; ++j) {
-      const float y2 = fmaf(t[j], k2, b2);
-      const float e = exp2f(y2);  // 0 for masked (-inf) columns
+    for (int j = 0; j < N; ++j) {
+      const float y2 = fmaf(v[j], k2, b2);
+      const float e = ex2_approx(y2);  // 0 for masked (-inf) columns
       s4[j & 3] += e;
       w4[j & 3] = fmaf(e, e > 0.f ? y2 : 0.f, w4[j & 3]);
     }
@@ -222,30 +269,69 @@ __device__ inline void chunk_stats(const float (&v)[32], int nv, int col0, float
   }
 }
 
+// One block of NCH 16-column chunks starting at chunk `ch` of the accumulator
+// at `tl`: load, statistics, logits copy and child gathers.
+template <int NCH>
+__device__ inline void epi_block(const EpiArgs& ea, uint32_t tl, int ch, int ncol, int n0, int r, int b, bool use,
+                                 float k2, bool tempered, int c_beg, uint64_t hits, float& m, int& arg, float& s,
+                                 float& w2, bool& nan_seen) {
+  float v[NCH * 16];
+  tc::tmem_ld16n<NCH>(tl + ch * 16, v);
+  if (!use) return;
+  const int c0 = ch * 16;
+  const int nv = min(NCH * 16, ncol - c0);
+  if (ea.logits && nv > 0) {
+    float* dst = ea.logits + static_cast<size_t>(r) * ea.V + n0 + c0;
+#pragma unroll
+    for (int j = 0; j < NCH * 16; ++j)
+      if (j < nv) dst[j] = v[j];
+  }
+  for (uint64_t hm = hits; hm; hm &= hm - 1) {
+    const int k = __ffsll(static_cast<long long>(hm)) - 1;
+    const int c = c_beg + k;
+    const int rel = ea.tokens[static_cast<size_t>(b) * ea.T + c] - (n0 + c0);
+    if (rel >= 0 && rel < nv) {
+      float z = 0.f;
+#pragma unroll
+      for (int j = 0; j < NCH * 16; ++j) z = (j == rel) ? v[j] : z;
+      ea.child_z[static_cast<size_t>(b) * ea.T + c] = z;
+    }
+  }
+  block_stats<NCH>(v, nv, n0 + c0, k2, tempered, m, arg, s, w2, nan_seen);
+}
+
+__device__ inline bool failed(const volatile int* f) { return *f != 0; }
+
 template <int BN>
 __global__ void __launch_bounds__(kTcThreads, 1) verify_tc_kernel(const __grid_constant__ CUtensorMap tma_x,
                                                                  const __grid_constant__ CUtensorMap tma_w, int H,
-                                                                 int n_mt, TcShape sh, EpiArgs ea) {
+                                                                 TcShape sh, EpiArgs ea) {
   extern __shared__ __align__(1024) unsigned char tc_smem_raw[];
-  const uint32_t X_BYTES = static_cast<uint32_t>(sh.xr) * BK * 2;
   constexpr uint32_t W_BYTES = BN * BK * 2;
-  constexpr uint32_t TMEM_COLS = BN <= 32 ? 32 : BN <= 64 ? 64 : BN <= 128 ? 128 : 256;
+  constexpr int ACC_STRIDE = (BN + 31) / 32 * 32;  // TMEM columns from one accumulator to the other
+  constexpr uint32_t TMEM_COLS = 2 * ACC_STRIDE <= 64 ? 64 : 2 * ACC_STRIDE <= 128 ? 128 : 2 * ACC_STRIDE <= 256 ? 256 : 512;
+  constexpr int NCH = BN / 16;  // 16-column chunks of a tile
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(tc_smem_raw) + 1023) & ~uintptr_t(1023));
-  unsigned char* xsm = smem;                                  // [sx][xr rows x 128 B]
-  unsigned char* wsm = smem + sh.sx * X_BYTES;                // [sw][BN rows x 128 B]
+  unsigned char* xsm = smem;                             // [sx][128 rows x 128 B]
+  unsigned char* wsm = smem + sh.sx * kXStageBytes;      // [sw][BN rows x 128 B]
   uint64_t* wfull = reinterpret_cast<uint64_t*>(wsm + sh.sw * W_BYTES);
-  uint64_t* wempty = wfull + kMaxStages;
-  uint64_t* xfull = wempty + kMaxStages;
-  uint64_t* xempty = xfull + kMaxStages;
-  uint64_t* accb = xempty + kMaxStages;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accb + 1);
-  float* xh = reinterpret_cast<float*>(tmem_slot + 4);        // [5][BM] upper-half row statistics
+  uint64_t* wempty = wfull + kMaxStagesW;
+  uint64_t* xfull = wempty + kMaxStagesW;
+  uint64_t* xempty = xfull + kMaxStagesX;
+  uint64_t* acc_full = xempty + kMaxStagesX;
+  uint64_t* acc_empty = acc_full + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 2);
+  float* xh = reinterpret_cast<float*>(tmem_slot + 4);  // [2][kColGroups-1][5][BM] statistics of groups 1..
   __shared__ int s_fail;
 
-  const int tile = blockIdx.x;
-  const int m_t = tile % n_mt, n_t = tile / n_mt;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nk = cdiv(H, BK);
+  const int qr = sh.qr;
+  // In the memory-bound GEMM (one row tile) CTAs start their K loops at
+  // different blocks, spreading the concurrent requests over more DRAM pages;
+  // the compute-bound one keeps the CTAs that share a weight tile in step, so
+  // the tile is still in L2 for all of them
+  const int rot = sh.n_mt == 1 ? static_cast<int>((static_cast<long>(blockIdx.x) * nk) / gridDim.x) : 0;
 
   if (threadIdx.x == 0) {
     s_fail = 0;
@@ -257,7 +343,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) verify_tc_kernel(const __grid_c
       tc::mbar_init(xfull + s, 1);
       tc::mbar_init(xempty + s, 1);
     }
-    tc::mbar_init(accb, 1);
+    for (int a = 0; a < 2; ++a) {
+      tc::mbar_init(acc_full + a, 1);
+      tc::mbar_init(acc_empty + a, kEpiWarps);
+    }
     tc::fence_mbar_init();
     tc::prefetch_tmap(&tma_x);
     tc::prefetch_tmap(&tma_w);
@@ -266,161 +355,203 @@ __global__ void __launch_bounds__(kTcThreads, 1) verify_tc_kernel(const __grid_c
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t taddr = *tmem_slot;
+  pdl_trigger();  // the merge kernel may take its place early (it waits for this grid)
 
   if (warp == kWarpW) {
     // lm_head is a constant input of the step: its stream starts before the
     // wait on the preceding kernel
     if (lane == 0) {
-      for (int i = 0; i < nk; ++i) {
-        const int s = i % sh.sw;
-        const uint32_t ph = (i / sh.sw) & 1;
-        if (!tc::mbar_wait(wempty + s, ph ^ 1)) { s_fail = 1; break; }
-        tc::mbar_expect_tx(wfull + s, W_BYTES);
-        tc::tma_load_2d(smem_u32(wsm + s * W_BYTES), &tma_w, i * BK, n_t * BN, wfull + s);
+      int i = 0;
+      bool run = true;
+      for (int t = blockIdx.x; t < sh.n_tiles && run; t += gridDim.x) {
+        const int n_t = t / sh.n_mt;
+        for (int k = 0; k < nk; ++k, ++i) {
+          const int s = i % sh.sw;
+          if (failed(&s_fail) || !tc::mbar_wait(wempty + s, ((i / sh.sw) & 1) ^ 1)) { s_fail = 1; run = false; break; }
+          tc::mbar_expect_tx(wfull + s, W_BYTES);
+          tc::tma_load_2d(smem_u32(wsm + s * W_BYTES), &tma_w, ((k + rot) % nk) * BK, n_t * BN, wfull + s);
+        }
       }
     }
     __syncwarp();
   } else if (warp == kWarpX) {
     pdl_wait();
     if (lane == 0) {
-      for (int i = 0; i < nk; ++i) {
-        const int s = i % sh.sx;
-        const uint32_t ph = (i / sh.sx) & 1;
-        if (!tc::mbar_wait(xempty + s, ph ^ 1)) { s_fail = 1; break; }
-        tc::mbar_expect_tx(xfull + s, X_BYTES);
-        tc::tma_load_2d(smem_u32(xsm + s * X_BYTES), &tma_x, i * BK, m_t * BM, xfull + s);
+      int i = 0;
+      bool run = true;
+      for (int t = blockIdx.x; t < sh.n_tiles && run; t += gridDim.x) {
+        const int row0 = (t % sh.n_mt) * 4 * qr;
+        for (int k = 0; k < nk; ++k, ++i) {
+          const int s = i % sh.sx;
+          if (failed(&s_fail) || !tc::mbar_wait(xempty + s, ((i / sh.sx) & 1) ^ 1)) { s_fail = 1; run = false; break; }
+          tc::mbar_expect_tx(xfull + s, 4u * qr * BK * 2);
+          for (int q = 0; q < 4; ++q)
+            tc::tma_load_2d(smem_u32(xsm + s * kXStageBytes + q * 32 * BK * 2), &tma_x, ((k + rot) % nk) * BK, row0 + q * qr,
+                            xfull + s);
+        }
       }
     }
     __syncwarp();
   } else if (warp == kWarpMma) {
     if (lane == 0) {
       constexpr uint32_t idesc = tc::idesc_bf16_f32(BM, BN);
-      for (int i = 0; i < nk; ++i) {
-        const int sw = i % sh.sw, sx = i % sh.sx;
-        if (!tc::mbar_wait(wfull + sw, (i / sh.sw) & 1) || !tc::mbar_wait(xfull + sx, (i / sh.sx) & 1)) {
-          s_fail = 1;
-          break;
-        }
+      int i = 0, jl = 0;
+      bool run = true;
+      for (int t = blockIdx.x; t < sh.n_tiles && run; t += gridDim.x, ++jl) {
+        const int a = jl & 1;
+        if (failed(&s_fail) || !tc::mbar_wait(acc_empty + a, ((jl >> 1) & 1) ^ 1)) { s_fail = 1; break; }
         tc::fence_after_sync();
-        const uint32_t sa = smem_u32(xsm + sx * X_BYTES), sb = smem_u32(wsm + sw * W_BYTES);
+        const uint32_t d = taddr + a * ACC_STRIDE;
+        for (int k = 0; k < nk; ++k, ++i) {
+          const int sw = i % sh.sw, sx = i % sh.sx;
+          if (failed(&s_fail) || !tc::mbar_wait(wfull + sw, (i / sh.sw) & 1) ||
+              !tc::mbar_wait(xfull + sx, (i / sh.sx) & 1)) {
+            s_fail = 1;
+            run = false;
+            break;
+          }
+          tc::fence_after_sync();
+          const uint32_t sa = smem_u32(xsm + sx * kXStageBytes), sb = smem_u32(wsm + sw * W_BYTES);
 #pragma unroll
-        for (int k = 0; k < BK / 16; ++k)
-          tc::mma_bf16(taddr, tc::smem_desc_sw128(sa + k * 32), tc::smem_desc_sw128(sb + k * 32), idesc,
-                       (i | k) != 0);
-        tc::mma_commit(wempty + sw);
-        tc::mma_commit(xempty + sx);
+          for (int kk = 0; kk < BK / 16; ++kk)
+            tc::mma_bf16(d, tc::smem_desc_sw128(sa + kk * 32), tc::smem_desc_sw128(sb + kk * 32), idesc,
+                         (k | kk) != 0);
+          tc::mma_commit(wempty + sw);
+          tc::mma_commit(xempty + sx);
+        }
+        if (run) tc::mma_commit(acc_full + a);  // fires once every MMA of the tile has completed
       }
-      tc::mma_commit(accb);  // fires once every issued MMA has completed
     }
     __syncwarp();
   } else {
     pdl_wait();
-    // ---- epilogue: thread = one tree-node row, one column group of the tile ----
+    // ---- epilogue: thread = one tree row (lane < qr) of its quadrant, one column group ----
     const int quad = warp & 3, grp = warp >> 2;
-    const int row = quad * 32 + lane;
-    const int r = m_t * BM + row;
-    const bool valid_row = r < ea.R;
-    const uint32_t tl = taddr + (static_cast<uint32_t>(quad * 32) << 16);
-    const int n0 = n_t * BN;
-    const int ncol = min(BN, ea.V - n0);  // valid columns of this tile
-    constexpr int NCH = (BN + 31) / 32;
     const int ch0 = grp * NCH / kColGroups, ch1 = (grp + 1) * NCH / kColGroups;
-    // While the MMAs run: which of this row's children have their token in
-    // this group's columns (bit k: child c_beg + k; a node has < 64 children).
-    int b = 0, c_beg = 0;
-    uint64_t hits = 0;
-    if (valid_row) {
-      b = r / ea.T;
-      const int node = r % ea.T;
-      c_beg = ea.tr.child_start[node];
-      const int c_cnt = ea.tr.child_count[node];
-      const int32_t* tok = ea.tokens + static_cast<size_t>(b) * ea.T + c_beg;
-      const int lo = n0 + ch0 * 32, hi = n0 + min(ncol, ch1 * 32);
-      for (int k0 = 0; k0 < c_cnt; k0 += 8) {
-        int t[8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) t[u] = k0 + u < c_cnt ? tok[k0 + u] : -1;
-#pragma unroll
-        for (int u = 0; u < 8; ++u)
-          if (t[u] >= lo && t[u] < hi) hits |= 1ull << (k0 + u);
-      }
-    }
-    const bool ok = tc::mbar_wait(accb, 0);
-    tc::fence_after_sync();
     const bool tempered = ea.inv_tau > 0.f;
     const float k2 = ea.inv_tau * kLog2e;
-    float m = -INFINITY, s = 0.f, w2 = 0.f;
-    int arg = n0 + ch0 * 32;
-    bool nan_seen = false;
-#pragma unroll 1
-    for (int ch = ch0; ch < ch1; ++ch) {
-      const int c0 = ch * 32;
-      float v[32];
-      tc::tmem_ld32(tl + c0, v);
-      if (!valid_row || !ok) continue;
-      const int nv = min(32, ncol - c0);
-      chunk_stats(v, nv, n0 + c0, k2, tempered, m, arg, s, w2, nan_seen);
-      if (ea.logits) {
-        float* dst = ea.logits + static_cast<size_t>(r) * ea.V + n0 + c0;
+    int jl = 0;
+    bool ok = true;
+    float run_m = -INFINITY, run_s = 0.f, run_w2 = 0.f;  // this CTA's tiles folded (one row tile)
+    int run_arg = 0x7fffffff;
+    bool run_nan = false;
+    for (int t = blockIdx.x; t < sh.n_tiles; t += gridDim.x, ++jl) {
+      const int a = jl & 1;
+      const int m_t = t % sh.n_mt, n_t = t / sh.n_mt;
+      const int r = m_t * 4 * qr + quad * qr + lane;
+      const bool valid_row = lane < qr && r < ea.R;
+      const uint32_t tl = taddr + (static_cast<uint32_t>(quad * 32) << 16) + a * ACC_STRIDE;
+      const int n0 = n_t * BN;
+      const int ncol = min(BN, ea.V - n0);  // valid columns of this tile
+      // While the MMAs run: which of this row's children have their token in
+      // this group's columns (bit k: child c_beg + k; a node has < 64 children).
+      int b = 0, c_beg = 0;
+      uint64_t hits = 0;
+      if (valid_row) {
+        b = r / ea.T;
+        const int node = r % ea.T;
+        c_beg = ea.tr.child_start[node];
+        const int c_cnt = ea.tr.child_count[node];
+        const int32_t* tok = ea.tokens + static_cast<size_t>(b) * ea.T + c_beg;
+        const int lo = n0 + ch0 * 16, hi = n0 + min(ncol, ch1 * 16);
+        for (int k0 = 0; k0 < c_cnt; k0 += 8) {
+          int tk[8];
 #pragma unroll
-        for (int j = 0; j < 32; ++j)
-          if (j < nv) dst[j] = v[j];
-      }
-      for (uint64_t hm = hits; hm; hm &= hm - 1) {
-        const int k = __ffsll(static_cast<long long>(hm)) - 1;
-        const int c = c_beg + k;
-        const int rel = ea.tokens[static_cast<size_t>(b) * ea.T + c] - (n0 + c0);
-        if (rel >= 0 && rel < nv) {
-          float z = 0.f;
+          for (int u = 0; u < 8; ++u) tk[u] = k0 + u < c_cnt ? tok[k0 + u] : -1;
 #pragma unroll
-          for (int j = 0; j < 32; ++j) z = (j == rel) ? v[j] : z;
-          ea.child_z[static_cast<size_t>(b) * ea.T + c] = z;
+          for (int u = 0; u < 8; ++u)
+            if (tk[u] >= lo && tk[u] < hi) hits |= 1ull << (k0 + u);
         }
       }
-    }
-    // groups 1.. hand their statistics to group 0, which merges them in
-    // column order (ties keep the lower column) and writes the tile's partial
-    if (kColGroups > 1) {
-      if (grp > 0) {
-        float* x = xh + (grp - 1) * 5 * BM;
-        x[row] = m;
-        x[BM + row] = s;
-        x[2 * BM + row] = w2;
-        x[3 * BM + row] = __int_as_float(arg);
-        x[4 * BM + row] = nan_seen ? 1.f : 0.f;
-      }
-      asm volatile("bar.sync 1, %0;" ::"n"(kEpiWarps * 32) : "memory");
-    }
-    if (grp == 0 && valid_row) {
-      float M = m;
-      for (int g = 1; g < kColGroups; ++g) {
-        const float mg = xh[(g - 1) * 5 * BM + row];
-        if (mg > M) {
-          M = mg;
-          arg = __float_as_int(xh[(g - 1) * 5 * BM + 3 * BM + row]);
-        }
-        nan_seen |= xh[(g - 1) * 5 * BM + 4 * BM + row] != 0.f;
-      }
-      float S = 0.f, W2 = 0.f;
-      if (tempered) {
-        if (s > 0.f) {
-          const float d = (m - M) * k2, sc = exp2f(d);
-          S += sc * s;
-          W2 += sc * fmaf(d, s, w2);
-        }
-        for (int g = 1; g < kColGroups; ++g) {
-          const float* x = xh + (g - 1) * 5 * BM;
-          const float mg = x[row], sg = x[BM + row], wg = x[2 * BM + row];
-          if (sg > 0.f) {
-            const float d = (mg - M) * k2, sc = exp2f(d);
-            S += sc * sg;
-            W2 += sc * fmaf(d, sg, wg);
+      ok = ok && __all_sync(0xffffffffu, !failed(&s_fail) && tc::mbar_wait(acc_full + a, (jl >> 1) & 1));
+      tc::fence_after_sync();
+      float m = -INFINITY, s = 0.f, w2 = 0.f;
+      int arg = n0 + ch0 * 16;
+      bool nan_seen = false;
+      if (ok) {
+        const bool use = valid_row;
+        for (int ch = ch0; ch < ch1; ch += 4) {
+          switch (min(4, ch1 - ch)) {
+            case 4: epi_block<4>(ea, tl, ch, ncol, n0, r, b, use, k2, tempered, c_beg, hits, m, arg, s, w2, nan_seen); break;
+            case 3: epi_block<3>(ea, tl, ch, ncol, n0, r, b, use, k2, tempered, c_beg, hits, m, arg, s, w2, nan_seen); break;
+            case 2: epi_block<2>(ea, tl, ch, ncol, n0, r, b, use, k2, tempered, c_beg, hits, m, arg, s, w2, nan_seen); break;
+            default: epi_block<1>(ea, tl, ch, ncol, n0, r, b, use, k2, tempered, c_beg, hits, m, arg, s, w2, nan_seen); break;
           }
         }
       }
-      if (nan_seen) S = __int_as_float(0x7fc00000);
-      ea.part[static_cast<size_t>(r) * ea.n_nt + n_t] = make_float4(M, S, W2 * kLn2, __int_as_float(arg));
-      if ((!ok || s_fail) && ea.dev_status) atomicOr(ea.dev_status + b, MEDUSA_DEV_TIMEOUT);
+      // the accumulator may take the next tile's MMAs once every warp has read it
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(acc_empty + a);
+      // groups 1.. hand their statistics to group 0, which merges them in
+      // column order (ties keep the lower column) and writes the tile's partial
+      float* xb = xh + a * (kColGroups - 1) * 5 * BM;
+      const int row = quad * 32 + lane;
+      if (kColGroups > 1) {
+        if (grp > 0) {
+          float* x = xb + (grp - 1) * 5 * BM;
+          x[row] = m;
+          x[BM + row] = s;
+          x[2 * BM + row] = w2;
+          x[3 * BM + row] = __int_as_float(arg);
+          x[4 * BM + row] = nan_seen ? 1.f : 0.f;
+        }
+        asm volatile("bar.sync 1, %0;" ::"n"(kEpiWarps * 32) : "memory");
+      }
+      if (grp == 0 && valid_row) {
+        float M = m;
+        for (int g = 1; g < kColGroups; ++g) {
+          const float mg = xb[(g - 1) * 5 * BM + row];
+          if (mg > M) {
+            M = mg;
+            arg = __float_as_int(xb[(g - 1) * 5 * BM + 3 * BM + row]);
+          }
+          nan_seen |= xb[(g - 1) * 5 * BM + 4 * BM + row] != 0.f;
+        }
+        float S = 0.f, W2 = 0.f;
+        if (tempered) {
+          if (s > 0.f) {
+            const float d = (m - M) * k2, sc = ex2_approx(d);
+            S += sc * s;
+            W2 += sc * fmaf(d, s, w2);
+          }
+          for (int g = 1; g < kColGroups; ++g) {
+            const float* x = xb + (g - 1) * 5 * BM;
+            const float mg = x[row], sg = x[BM + row], wg = x[2 * BM + row];
+            if (sg > 0.f) {
+              const float d = (mg - M) * k2, sc = ex2_approx(d);
+              S += sc * sg;
+              W2 += sc * fmaf(d, sg, wg);
+            }
+          }
+        }
+        if (sh.n_mt > 1) {
+          if (nan_seen) S = __int_as_float(0x7fc00000);
+          ea.part[static_cast<size_t>(r) * ea.n_nt + n_t] = make_float4(M, S, W2 * kLn2, __int_as_float(arg));
+        } else {
+          // one row tile: every tile of this CTA has the same rows, so the CTA
+          // folds its tiles into one partial (ties keep the lower column)
+          if (M > run_m || (M == run_m && arg < run_arg)) {
+            if (tempered && run_s > 0.f) {
+              const float d = (run_m - M) * k2, sc = ex2_approx(d);
+              run_w2 = sc * fmaf(d, run_s, run_w2);
+              run_s *= sc;
+            }
+            run_m = M;
+            run_arg = arg;
+          }
+          if (tempered && S > 0.f) {
+            const float d = (M - run_m) * k2, sc = ex2_approx(d);
+            run_s += sc * S;
+            run_w2 += sc * fmaf(d, S, W2);
+          }
+          run_nan |= nan_seen;
+          if (t + static_cast<int>(gridDim.x) >= sh.n_tiles)
+            ea.part[static_cast<size_t>(r) * ea.n_nt + blockIdx.x] =
+                make_float4(run_m, run_nan ? __int_as_float(0x7fc00000) : run_s, run_w2 * kLn2, __int_as_float(run_arg));
+        }
+        if ((!ok || failed(&s_fail)) && ea.dev_status) atomicOr(ea.dev_status + b, MEDUSA_DEV_TIMEOUT);
+      }
     }
   }
   tc::fence_before_sync();
@@ -544,9 +675,10 @@ __device__ inline float4 merge_row(const float4* __restrict__ pr, int n_nt, floa
 struct AcceptArgs {
   medusa_tree_dev tr;
   const int32_t* tokens;
-  const float4* part;  // [R, n_nt] tile statistics
+  const float4* part;  // [R, n_nt] statistics partials (n_nt of them per row)
   int n_nt, R;
   float4* rowst;       // [R] merged statistics
+  unsigned char* acc;  // [R] typical-acceptance test of each node against its parent (root: 1)
   int* tickets;        // [B] self-resetting
   const float* child_z;
   float inv_tau, thr, alpha;
@@ -561,111 +693,129 @@ struct AcceptArgs {
 };
 
 // ------------------------------------------------------------------------
-// K6b: typical acceptance of request b, longest kept prefix, next root
-// (whole CTA; the request's merged statistics are in a.rowst).
+// K6b: longest kept prefix of request b and the next root (whole CTA; every
+// node's own acceptance test is in a.acc, the merged statistics in a.rowst).
+// A node is kept when it and all its ancestors passed; the deepest kept node
+// wins, ties to the lowest canonical index.
 // ------------------------------------------------------------------------
 __device__ void accept_request(const AcceptArgs& a, int b, unsigned char* s_acc, const int16_t* s_par,
-                               const int16_t* s_dep, int* s_sc) {
+                               const int16_t* s_dep, const int16_t* s_fp, int* s_chain, int* s_best) {
   const medusa_tree_dev& tr = a.tr;
   const int T = tr.T;
   const size_t base = static_cast<size_t>(b) * T;
-  int& s_best = s_sc[0];
-  int& s_path = s_sc[1];
-  int& s_nan = s_sc[2];
-  if (threadIdx.x == 0) { s_best = 0; s_path = 0x7fffffff; s_nan = 0; }
-  __syncthreads();
-  for (int c = threadIdx.x; c < T; c += blockDim.x) {
-    const float4 own = __ldcg(a.rowst + base + c);
-    if (a.node_H) {
-      float H = 0.f;
-      if (a.inv_tau > 0.f) H = logf(own.y) - own.z / own.y;
-      a.node_H[base + c] = H;
-    }
-    if (own.x != own.x || own.y != own.y) s_nan = 1;
-    if (c == 0) {
-      s_acc[0] = 1;
-      if (a.node_p) a.node_p[base] = 1.f;
-      continue;
-    }
-    const float4 par = __ldcg(a.rowst + base + s_par[c]);
-    const int32_t tok = a.tokens[base + c];
-    bool acc;
-    float p;
-    if (a.inv_tau > 0.f) {
-      const float H = logf(par.y) - par.z / par.y;
-      p = expf((a.child_z[base + c] - par.x) * a.inv_tau) / par.y;
-      acc = p > fminf(a.thr, a.alpha * expf(-H));
-    } else {
-      acc = tok == __float_as_int(par.w);
-      p = acc ? 1.f : 0.f;
-    }
-    s_acc[c] = acc ? 1 : 0;
-    if (a.node_p) a.node_p[base + c] = p;
-  }
+  if (threadIdx.x == 0) *s_best = 0;
+  for (int c = threadIdx.x; c < T; c += blockDim.x) s_acc[c] = __ldcg(a.acc + base + c);
   __syncthreads();
   for (int d = 1; d <= tr.dmax; ++d) {
     for (int c = threadIdx.x; c < T; c += blockDim.x)
       if (s_dep[c] == d) s_acc[c] = s_acc[c] && s_acc[s_par[c]];
     __syncthreads();
   }
-  // deepest kept node, ties to the lowest canonical index
   int key = 0xFFFF;  // root: depth 0, index 0
   for (int c = threadIdx.x; c < T; c += blockDim.x)
     if (s_acc[c]) key = max(key, (static_cast<int>(s_dep[c]) << 16) | (0xFFFF - c));
   for (int o = 16; o > 0; o >>= 1) key = max(key, __shfl_xor_sync(0xffffffffu, key, o));
-  if ((threadIdx.x & 31) == 0) atomicMax(&s_best, key);
+  if ((threadIdx.x & 31) == 0) atomicMax(s_best, key);
   __syncthreads();
-  const int best = 0xFFFF - (s_best & 0xFFFF);
-  for (int p = threadIdx.x; p < tr.P; p += blockDim.x) {
-    const int leaf = tr.leaf[p];
-    if ((tr.mask[static_cast<size_t>(leaf) * tr.mask_words + best / 32] >> (best % 32)) & 1u) atomicMin(&s_path, p);
+  const int best = 0xFFFF - (*s_best & 0xFFFF);
+  const int a_len = s_dep[best];
+  if (threadIdx.x == 0) {
+    int node = best;
+    for (int d = a_len; d >= 0; --d) {
+      s_chain[d] = node;
+      node = s_par[node];
+    }
   }
   __syncthreads();
-  // accepted tokens root..best, read off best's ancestor-mask row
-  const int a_len = s_dep[best];
+  // accepted tokens root..best, -1 past the winner
   int32_t* out = a.accepted_tokens + static_cast<size_t>(b) * (tr.dmax + 1);
-  for (int t = threadIdx.x; t < T; t += blockDim.x)
-    if ((tr.mask[static_cast<size_t>(best) * tr.mask_words + t / 32] >> (t % 32)) & 1u)
-      out[s_dep[t]] = a.tokens[base + t];
-  for (int d = a_len + 1 + threadIdx.x; d <= tr.dmax; d += blockDim.x) out[d] = -1;
-  if (threadIdx.x == 0) {
+  for (int d = threadIdx.x; d <= tr.dmax; d += blockDim.x) out[d] = d <= a_len ? a.tokens[base + s_chain[d]] : -1;
+  if (threadIdx.x == 32) {  // a second warp, beside the token reads of the first
+    a.next_root[b] = __float_as_int(__ldcg(a.rowst + base + best).w);
     a.accept_len[b] = a_len;
     a.best_node[b] = best;
-    a.best_path[b] = s_path;
-    a.next_root[b] = __float_as_int(__ldcg(a.rowst + base + best).w);
-    if (s_nan && a.dev_status) atomicOr(a.dev_status + b, MEDUSA_DEV_NAN);
+    a.best_path[b] = s_fp[best];
   }
   __syncthreads();
 }
 
 // ------------------------------------------------------------------------
 // K6: merge each node's tile statistics (warp per node, kMergeRows nodes per
-// CTA, tiles in fixed order); the last CTA to finish a request's nodes
-// (ticket per request) then runs that request's acceptance.
+// CTA), then test the node's children against them: at temperature > 0
+// child c passes when p(c) = softmax(z/tau)[token c] exceeds
+// min(threshold, alpha * exp(-H)) with H the entropy of the same
+// distribution; at temperature 0 when its token is the argmax.  The last CTA
+// to finish a request's nodes (ticket per request) then runs K6b for it.
 // ------------------------------------------------------------------------
 constexpr int kMergeRows = 8;
 
 __global__ void __launch_bounds__(kMergeRows * 32) merge_accept_kernel(AcceptArgs a) {
-  // shared: parent[T], depth[T] (int16; the tree tables are constant, so they are
-  // read before the wait on the preceding kernel), then acc[T] bytes
+  // shared: parent[T], depth[T], first path[T] (int16; the tree tables are constant,
+  // so they are read before the wait on the preceding kernel), then kept[T] bytes
   extern __shared__ __align__(16) unsigned char accept_smem[];
   const int T = a.tr.T;
   int16_t* s_par = reinterpret_cast<int16_t*>(accept_smem);
   int16_t* s_dep = s_par + T;
-  unsigned char* s_acc = reinterpret_cast<unsigned char*>(s_dep + T);
-  __shared__ int s_sc[3];
+  int16_t* s_fp = s_dep + T;
+  unsigned char* s_acc = reinterpret_cast<unsigned char*>(s_fp + T);
+  __shared__ int s_chain[MEDUSA_MAX_DEPTH + 1];
+  __shared__ int s_best;
   __shared__ int s_last;
   for (int c = threadIdx.x; c < T; c += blockDim.x) {
     s_par[c] = static_cast<int16_t>(a.tr.parent[c]);
     s_dep[c] = static_cast<int16_t>(a.tr.depth[c]);
+    s_fp[c] = static_cast<int16_t>(a.tr.first_path[c]);
+  }
+  const int r0 = blockIdx.x * kMergeRows, r1 = min(a.R, r0 + kMergeRows);
+  const int r = r0 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  int c_beg = 0, c_cnt = 0;
+  if (r < r1) {
+    const int node = r % T;
+    c_beg = a.tr.child_start[node];
+    c_cnt = a.tr.child_count[node];
   }
   pdl_wait();
   pdl_trigger();
-  const int r0 = blockIdx.x * kMergeRows, r1 = min(a.R, r0 + kMergeRows);
-  const int r = r0 + (threadIdx.x >> 5);
   if (r < r1) {
+    const int b = r / T, node = r % T;
+    const size_t base = static_cast<size_t>(b) * T;
+    // the first 32 children's tokens and logits load beside the partials
+    int tok = 0;
+    float cz = 0.f;
+    if (lane < c_cnt) {
+      tok = a.tokens[base + c_beg + lane];
+      cz = a.child_z[base + c_beg + lane];
+    }
     const float4 v = merge_row(a.part + static_cast<size_t>(r) * a.n_nt, a.n_nt, a.inv_tau);
-    if ((threadIdx.x & 31) == 0) a.rowst[r] = v;
+    const bool tempered = a.inv_tau > 0.f;
+    const float H = tempered ? logf(v.y) - v.z / v.y : 0.f;
+    const float thr = fminf(a.thr, a.alpha * expf(-H));
+    if (lane == 0) {
+      a.rowst[r] = v;
+      if (a.node_H) a.node_H[base + node] = H;
+      if (node == 0) {
+        a.acc[base] = 1;
+        if (a.node_p) a.node_p[base] = 1.f;
+      }
+      if ((v.x != v.x || v.y != v.y) && a.dev_status) atomicOr(a.dev_status + b, MEDUSA_DEV_NAN);
+    }
+    for (int k = lane; k < c_cnt; k += 32) {
+      if (k >= 32) {
+        tok = a.tokens[base + c_beg + k];
+        cz = a.child_z[base + c_beg + k];
+      }
+      bool pass;
+      float p;
+      if (tempered) {
+        p = expf((cz - v.x) * a.inv_tau) / v.y;
+        pass = p > thr;
+      } else {
+        pass = tok == __float_as_int(v.w);
+        p = pass ? 1.f : 0.f;
+      }
+      a.acc[base + c_beg + k] = pass ? 1 : 0;
+      if (a.node_p) a.node_p[base + c_beg + k] = p;
+    }
   }
   __threadfence();
   __syncthreads();
@@ -675,7 +825,7 @@ __global__ void __launch_bounds__(kMergeRows * 32) merge_accept_kernel(AcceptArg
     __syncthreads();
     if (s_last) {
       __threadfence();
-      accept_request(a, b, s_acc, s_par, s_dep, s_sc);
+      accept_request(a, b, s_acc, s_par, s_dep, s_fp, s_chain, &s_best);
       if (threadIdx.x == 0) a.tickets[b] = 0;  // ready for the next launch
     }
     __syncthreads();
@@ -683,21 +833,24 @@ __global__ void __launch_bounds__(kMergeRows * 32) merge_accept_kernel(AcceptArg
 }
 
 constexpr size_t kTcSmemMax = 227 * 1024 - 1024;  // the kernel's static shared memory takes 1 KB
-constexpr size_t kTcFixedBytes = 1024 + (4 * kMaxStages + 1) * 8 + 16 + kHalfXchgBytes;
+constexpr size_t kTcFixedBytes = 1024 + (2 * kMaxStagesW + 2 * kMaxStagesX + 4) * 8 + 16 + kXchgBytes;
 
 TcShape tc_shape(const VerifyPlan& p) {
   TcShape sh{};
   sh.BN = p.BN;
-  const int rows = p.n_mt == 1 ? p.R : BM;
-  sh.xr = std::min(BM, cdiv(rows, 8) * 8);
-  const size_t xb = static_cast<size_t>(sh.xr) * BK * 2, wb = static_cast<size_t>(p.BN) * BK * 2;
-  sh.sx = 4;
-  sh.sw = static_cast<int>(std::min<size_t>(kMaxStages, (kTcSmemMax - kTcFixedBytes - sh.sx * xb) / wb));
+  sh.qr = p.qr;
+  sh.n_mt = p.n_mt;
+  sh.n_tiles = p.n_tiles;
+  const size_t wb = static_cast<size_t>(p.BN) * BK * 2;
+  // three X stages (L2 latency); the rest of shared memory goes to the weight
+  // ring, which also carries the prefetch made before the dependency wait
+  sh.sx = 3;
+  sh.sw = static_cast<int>(std::min<size_t>(kMaxStagesW, (kTcSmemMax - kTcFixedBytes - sh.sx * kXStageBytes) / wb));
   return sh;
 }
 
 size_t tc_smem_bytes(const TcShape& sh) {
-  return kTcFixedBytes + static_cast<size_t>(sh.sx) * sh.xr * BK * 2 + static_cast<size_t>(sh.sw) * sh.BN * BK * 2;
+  return kTcFixedBytes + static_cast<size_t>(sh.sx) * kXStageBytes + static_cast<size_t>(sh.sw) * sh.BN * BK * 2;
 }
 
 template <int BN>
@@ -709,7 +862,7 @@ int launch_tc(const VerifyPlan& p, const CUtensorMap& mx, const CUtensorMap& mw,
   auto k = verify_tc_kernel<BN>;
   if (!ensure_dyn_smem(k, smem))
     return MEDUSA_ERR_CUDA;
-  if (launch_pdl(k, dim3(p.n_mt * p.n_nt), dim3(kTcThreads), smem, st, mx, mw, H, p.n_mt, sh, ea) != cudaSuccess) {
+  if (launch_pdl(k, dim3(p.grid), dim3(kTcThreads), smem, st, mx, mw, H, sh, ea) != cudaSuccess) {
     (void)cudaGetLastError();
     return MEDUSA_ERR_CUDA;
   }
@@ -763,11 +916,11 @@ MEDUSA_API int medusa_verify_accept(const medusa_tree* tree, const void* x, cons
   if (!ws || ws_bytes < w.bytes) return MEDUSA_ERR_WORKSPACE;
   auto st = reinterpret_cast<cudaStream_t>(stream);
   const float inv_tau = temperature > 0.f ? 1.f / temperature : 0.f;
-  EpiArgs ea{p.R, V, T, p.n_nt, tree_tokens, tree->dev, inv_tau, logits, w.part, w.child_z, dev_status};
+  EpiArgs ea{p.R, V, T, p.n_parts, tree_tokens, tree->dev, inv_tau, logits, w.part, w.child_z, dev_status};
 
   if (dtype == MEDUSA_BF16) {
     CUtensorMap mx, mw;
-    if (!make_tmap_bf16(&mx, x, p.R, H, tc_shape(p).xr) || !make_tmap_bf16(&mw, lm_head, V, H, p.BN))
+    if (!make_tmap_bf16(&mx, x, p.R, H, p.qr) || !make_tmap_bf16(&mw, lm_head, V, H, p.BN))
       return MEDUSA_ERR_CUDA;
     const int rc = dispatch_tc(p, mx, mw, H, ea, st);
     if (rc != MEDUSA_OK) return rc;
@@ -799,10 +952,10 @@ MEDUSA_API int medusa_verify_accept(const medusa_tree* tree, const void* x, cons
     }
     MEDUSA_LAUNCH_CHECK();
   }
-  AcceptArgs aa{tree->dev, tree_tokens, w.part, p.n_nt, p.R, w.rowst, w.tickets, w.child_z, inv_tau,
+  AcceptArgs aa{tree->dev, tree_tokens, w.part, p.n_parts, p.R, w.rowst, w.acc, w.tickets, w.child_z, inv_tau,
                 posterior_threshold, posterior_alpha, node_p, node_H, accept_len, best_path, best_node,
                 accepted_tokens, next_root, dev_status};
-  if (launch_pdl(merge_accept_kernel, dim3(cdiv(p.R, kMergeRows)), dim3(kMergeRows * 32), static_cast<size_t>(T) * 5,
+  if (launch_pdl(merge_accept_kernel, dim3(cdiv(p.R, kMergeRows)), dim3(kMergeRows * 32), static_cast<size_t>(T) * 7,
                  st, aa) != cudaSuccess) {
     (void)cudaGetLastError();
     return MEDUSA_ERR_CUDA;

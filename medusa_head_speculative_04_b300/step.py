@@ -98,14 +98,15 @@ class MedusaStep:
         self.verify(X, lm_head, temperature, threshold, alpha, stream=stream)
         self.commit(k_new, v_new, k_cache, v_cache, kv_len, stream=stream)
 
-    def capture(self, *args, prologue=None, stream: Optional[torch.cuda.Stream] = None, **kwargs):
+    def capture(self, *args, prologue=None, epilogue=None, stream: Optional[torch.cuda.Stream] = None, **kwargs):
         """Capture one whole step (the arguments of :meth:`run`) in a CUDA graph.
 
         The graph keeps the tensors it was captured with: refill them in place and
         ``replay()`` it to run the next step with one launch from the host.
-        ``prologue`` (a callable, or None) is captured just before the step, on the
-        same stream.  One eager step runs first, so its outputs change state
-        (``kv_len`` and the cache rows it commits) like any other step.
+        ``prologue`` and ``epilogue`` (callables, or None) are captured just before
+        and just after the step, on the same stream.  One eager step runs first, so
+        its outputs change state (``kv_len`` and the cache rows it commits) like any
+        other step.
         """
         cur = torch.cuda.current_stream(self.device)
         s = stream if stream is not None else torch.cuda.Stream(self.device)  # capture needs a side stream
@@ -114,11 +115,15 @@ class MedusaStep:
             if prologue is not None:
                 prologue()
             self.run(*args, **kwargs)     # sets the kernels' attributes outside the capture
+            if epilogue is not None:
+                epilogue()
         s.synchronize()
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=s):
             if prologue is not None:
                 prologue()
             self.run(*args, **kwargs)
+            if epilogue is not None:
+                epilogue()
         cur.wait_stream(s)
         return g
