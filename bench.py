@@ -73,6 +73,22 @@ def select_workload(args):
     return dataclasses.replace(wl, name=f"{wl.name}/tree={args.tree}", tree=tree)
 
 
+def max_over_ranks(x: float, device, ws: int) -> float:
+    """The largest of every rank's x (a timed region's length: the job ends with its slowest rank)."""
+    if ws <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_throughput(units_per_rank: int, ms: float, ws: int) -> float:
+    """Whole-job units per second: every rank processed units_per_rank in at most ms."""
+    return units_per_rank * ws / (ms / 1e3)
+
+
 def dist_env():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -264,11 +280,7 @@ def run_ours(args, ws, rank, local):
     if ws > 1:
         dist.barrier()
     clocks = sampler.stop()
-    ms = start.elapsed_time(end)
-    t = torch.tensor([ms], device=dev)
-    if ws > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    ms_max = float(t.item())
+    ms_max = max_over_ranks(start.elapsed_time(end), dev, ws)
     status = int(step.dev_status.max().item())
 
     # stage breakdown: a separate replay of the graph with events between the
@@ -371,10 +383,7 @@ def run_ours(args, ws, rank, local):
         with torch.cuda.stream(s):
             e1.record(s)
         torch.cuda.synchronize()
-        te = torch.tensor([e0.elapsed_time(e1)], device=dev)
-        if ws > 1:
-            dist.all_reduce(te, op=dist.ReduceOp.MAX)
-        return e2e_steps * wl.B * ws / (float(te.item()) / 1e3)
+        return replica_throughput(e2e_steps * wl.B, max_over_ranks(e0.elapsed_time(e1), dev, ws), ws)
 
     e2e_value = e2e_time(graphs=True)
     e2e_eager = e2e_time(graphs=False)
@@ -382,7 +391,7 @@ def run_ours(args, ws, rank, local):
     if rank != 0:
         return None
 
-    value = args.steps * wl.B * ws / (ms_max / 1e3)
+    value = replica_throughput(args.steps * wl.B, ms_max, ws)
     sb = step_bytes(wl, T)
     hbm, bf16, src = measured_peaks()
     heads_ms = statistics.mean(stage_ms["heads"]) if stage_ms["heads"] else None

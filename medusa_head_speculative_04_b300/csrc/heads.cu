@@ -15,6 +15,7 @@
 #include <mutex>
 
 #include "gemv.cuh"
+#include "tc.cuh"
 
 using namespace medusa;
 
@@ -41,6 +42,7 @@ template <int BMAX> struct Pass {
 // at the end.  K2 gives every head (block) the same number of CTAs, so each
 // CTA's rows lie inside one head and its top-k candidates belong to that head.
 struct HeadsPlan {
+  bool tc;      // vocabulary projection on the tensor cores (bf16, >= kTcMinRows rows, root given)
   int nblk;     // K heads (+1 for the lm_head root block)
   int cph;      // CTAs per block (head)
   int rpc;      // most rows one K2 CTA holds
@@ -66,10 +68,17 @@ size_t vocab_smem_bytes(int nb, int bmax, int H, int esize, int rpc, int cph, in
 
 int bmax_of(int nb) { return nb == 1 ? 1 : nb == 2 ? 2 : nb <= 4 ? 4 : nb <= 8 ? 8 : 16; }
 
+// From this many batch rows the CUDA-core dot products (B FMAs per weight
+// element) fall behind the weight stream, and z_k = W2_k u_k runs as a tcgen05
+// GEMM (M = batch rows, N = vocabulary) that writes the logits; K2 then only
+// selects the top-k from them.
+constexpr int kTcMinRows = 3;
+
 // Returns false when no split fits in shared memory.
-bool plan_heads(int B, int H, int V, int K, int with_root, int esize, int topk, HeadsPlan* out) {
+bool plan_heads(int B, int H, int V, int K, int with_root, int esize, int topk, bool allow_tc, HeadsPlan* out) {
   HeadsPlan p{};
   const int sms = device_sm_count();
+  p.tc = allow_tc && esize == 2 && !with_root && B >= kTcMinRows;
   p.nblk = K + (with_root ? 1 : 0);
   p.bgroup = static_cast<int>(std::min<size_t>(16, std::max<size_t>(1, kMaxXBytes / (static_cast<size_t>(H) * esize))));
   p.bgroup = std::min(p.bgroup, B);
@@ -101,21 +110,24 @@ bool plan_heads(int B, int H, int V, int K, int with_root, int esize, int topk, 
 
 struct HeadsWs {
   void* u;
+  float* z;  // [B, K, V] logits of the tensor-core path when the caller keeps none
   float* cand_v;
   int* cand_i;
   int* counters;
   size_t bytes;
 };
 
-HeadsWs carve_heads_ws(void* base, const HeadsPlan& p, int B, int H, int K, int topk, int esize) {
+HeadsWs carve_heads_ws(void* base, const HeadsPlan& p, int B, int H, int V, int K, int topk, int esize) {
   HeadsWs w{};
   size_t o = 0;
   auto take = [&](size_t n) { size_t s = o; o = align_up(o + n, 256); return s; };
   size_t ou = take(static_cast<size_t>(B) * K * H * esize);
   size_t ncand = static_cast<size_t>(p.nblk) * B * p.cph * topk;
   size_t ov = take(ncand * 4), oi = take(ncand * 4), oc = take(static_cast<size_t>(p.nblk) * 4);
+  size_t oz = p.tc ? take(static_cast<size_t>(B) * K * V * 4) : 0;
   char* c = static_cast<char*>(base);
   w.u = c ? c + ou : nullptr;
+  w.z = c && p.tc ? reinterpret_cast<float*>(c + oz) : nullptr;
   w.cand_v = c ? reinterpret_cast<float*>(c + ov) : nullptr;
   w.cand_i = c ? reinterpret_cast<int*>(c + oi) : nullptr;
   w.counters = c ? reinterpret_cast<int*>(c + oc) : nullptr;
@@ -180,13 +192,15 @@ __global__ void __launch_bounds__(kThreads) heads_fc_kernel(const T* __restrict_
 
 // K2: CTA j of block blk holds rows [j*V/cph, (j+1)*V/cph) of that block.
 // Block blk < K is head blk (weights W2_blk, activations u[:, blk]); block K is
-// lm_head on h (root).
-template <typename T, int BMAX>
+// lm_head on h (root).  FROMZ: the logits were computed by the tensor-core GEMM
+// (zsrc [B, K, V]) and the CTA only selects from its slice of them.
+template <typename T, int BMAX, bool FROMZ>
 __global__ void __launch_bounds__(kThreads) heads_vocab_kernel(
     const T* __restrict__ h, const T* __restrict__ u, const T* __restrict__ W2, const T* __restrict__ lm_head,
     int B, int b0, int nb, int H, int V, int K, int topk, int rpc, int cph,
     float* __restrict__ head_logits, int32_t* __restrict__ topk_ids, float* __restrict__ topk_vals,
-    int32_t* __restrict__ root_tok, float* __restrict__ cand_v, int* __restrict__ cand_i, int* __restrict__ counters) {
+    int32_t* __restrict__ root_tok, float* __restrict__ cand_v, int* __restrict__ cand_i, int* __restrict__ counters,
+    const float* __restrict__ zsrc) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   const int blk = blockIdx.x / cph, cta = blockIdx.x % cph;
   const bool is_root = blk == K;
@@ -210,14 +224,21 @@ __global__ void __launch_bounds__(kThreads) heads_vocab_kernel(
   const int v0 = static_cast<int>(static_cast<long>(cta) * V / cph);
   const int n = static_cast<int>(static_cast<long>(cta + 1) * V / cph) - v0;
   const int lr0 = warp * n / kWarps, lr1 = (warp + 1) * n / kWarps;  // this warp's local rows
-  prefetch_rows(W, v0 + lr0, lr1 - lr0, H);
+  if (!FROMZ) prefetch_rows(W, v0 + lr0, lr1 - lr0, H);
   pdl_wait();
   pdl_trigger();
-  stage_rows(xs, x, x_stride, nb, H);
+  if (FROMZ) {
+    for (int e = threadIdx.x; e < nb * n; e += blockDim.x) {
+      const int b = e / n, lr = e % n;
+      zs[static_cast<size_t>(b) * rpc + lr] = zsrc[(static_cast<size_t>(b0 + b) * K + blk) * V + v0 + lr];
+    }
+  } else {
+    stage_rows(xs, x, x_stride, nb, H);
+  }
   __syncthreads();
 
   constexpr int R = Pass<BMAX>::R;
-  for (int lr = lr0; lr < lr1; lr += R) {
+  for (int lr = lr0; lr < lr1 && !FROMZ; lr += R) {
     const int valid = min(R, lr1 - lr);
     float acc[R][BMAX];
     gemv_rows<T, BMAX, R, Pass<BMAX>::U>(W, static_cast<size_t>(v0 + lr), valid, H, xs, nb, acc);
@@ -275,9 +296,8 @@ __global__ void __launch_bounds__(kThreads) heads_vocab_kernel(
 }
 
 template <typename T, int BMAX>
-int launch_heads(const HeadsPlan& p, const HeadsWs& w, const T* h, const T* W1, const T* b1, const T* W2,
-                 const T* lm, int B, int b0, int nb, int H, int V, int K, int topk, float* head_logits,
-                 int32_t* topk_ids, float* topk_vals, int32_t* root_tok, cudaStream_t st) {
+int launch_fc(const HeadsPlan& p, const HeadsWs& w, const T* h, const T* W1, const T* b1, int b0, int nb, int H,
+              int K, cudaStream_t st) {
   const size_t xbytes = align_up(static_cast<size_t>(nb) * H * sizeof(T), 16);
   auto fc = heads_fc_kernel<T, BMAX>;
   if (!ensure_dyn_smem(fc, xbytes))
@@ -288,13 +308,20 @@ int launch_heads(const HeadsPlan& p, const HeadsWs& w, const T* h, const T* W1, 
     return MEDUSA_ERR_CUDA;
   }
   MEDUSA_LAUNCH_CHECK();
+  return MEDUSA_OK;
+}
+
+template <typename T, int BMAX, bool FROMZ>
+int launch_vocab(const HeadsPlan& p, const HeadsWs& w, const T* h, const T* W2, const T* lm, int B, int b0, int nb,
+                 int H, int V, int K, int topk, float* head_logits, int32_t* topk_ids, float* topk_vals,
+                 int32_t* root_tok, const float* zsrc, cudaStream_t st) {
   const size_t smem = vocab_smem_bytes(nb, BMAX, H, sizeof(T), p.rpc, p.cph, topk);
-  auto vk = heads_vocab_kernel<T, BMAX>;
+  auto vk = heads_vocab_kernel<T, BMAX, FROMZ>;
   if (!ensure_dyn_smem(vk, smem))
     return MEDUSA_ERR_CUDA;
   if (launch_pdl(vk, dim3(p.nblk * p.cph), dim3(kThreads), smem, st, h, static_cast<const T*>(w.u), W2, lm, B, b0, nb,
-                 H, V, K, topk, p.rpc, p.cph, head_logits, topk_ids, topk_vals, root_tok, w.cand_v, w.cand_i,
-                 w.counters) != cudaSuccess) {
+                 H, V, K, topk, p.rpc, p.cph, FROMZ ? nullptr : head_logits, topk_ids, topk_vals, root_tok, w.cand_v,
+                 w.cand_i, w.counters, zsrc) != cudaSuccess) {
     (void)cudaGetLastError();
     return MEDUSA_ERR_CUDA;
   }
@@ -302,18 +329,61 @@ int launch_heads(const HeadsPlan& p, const HeadsWs& w, const T* h, const T* W1, 
   return MEDUSA_OK;
 }
 
+template <typename T, bool FROMZ>
+int launch_vocab_nb(const HeadsPlan& p, const HeadsWs& w, const T* h, const T* W2, const T* lm, int B, int b0,
+                    int nb, int H, int V, int K, int topk, float* hl, int32_t* ids, float* vals, int32_t* root,
+                    const float* zsrc, cudaStream_t st) {
+  if (nb == 1) return launch_vocab<T, 1, FROMZ>(p, w, h, W2, lm, B, b0, nb, H, V, K, topk, hl, ids, vals, root, zsrc, st);
+  if (nb == 2) return launch_vocab<T, 2, FROMZ>(p, w, h, W2, lm, B, b0, nb, H, V, K, topk, hl, ids, vals, root, zsrc, st);
+  if (nb <= 4) return launch_vocab<T, 4, FROMZ>(p, w, h, W2, lm, B, b0, nb, H, V, K, topk, hl, ids, vals, root, zsrc, st);
+  if (nb <= 8) return launch_vocab<T, 8, FROMZ>(p, w, h, W2, lm, B, b0, nb, H, V, K, topk, hl, ids, vals, root, zsrc, st);
+  return launch_vocab<T, 16, FROMZ>(p, w, h, W2, lm, B, b0, nb, H, V, K, topk, hl, ids, vals, root, zsrc, st);
+}
+
+template <typename T>
+int launch_fc_nb(const HeadsPlan& p, const HeadsWs& w, const T* h, const T* W1, const T* b1, int b0, int nb, int H,
+                 int K, cudaStream_t st) {
+  if (nb == 1) return launch_fc<T, 1>(p, w, h, W1, b1, b0, nb, H, K, st);
+  if (nb == 2) return launch_fc<T, 2>(p, w, h, W1, b1, b0, nb, H, K, st);
+  if (nb <= 4) return launch_fc<T, 4>(p, w, h, W1, b1, b0, nb, H, K, st);
+  if (nb <= 8) return launch_fc<T, 8>(p, w, h, W1, b1, b0, nb, H, K, st);
+  return launch_fc<T, 16>(p, w, h, W1, b1, b0, nb, H, K, st);
+}
+
+int group_logits(const HeadsPlan&, const HeadsWs&, const float*, const float*, int, int, int, int, float*,
+                 cudaStream_t) {
+  return MEDUSA_ERR_UNSUPPORTED;  // the tensor-core path is bf16 only
+}
+int group_logits(const HeadsPlan&, const HeadsWs& w, const __nv_bfloat16*, const __nv_bfloat16* W2, int B, int H,
+                 int V, int K, float* z, cudaStream_t st) {
+  return launch_group_logits_bf16(w.u, B, K, W2, H, V, z, st);
+}
+
 template <typename T>
 int heads_dispatch(const HeadsPlan& p, const HeadsWs& w, const T* h, const T* W1, const T* b1, const T* W2,
                    const T* lm, int B, int H, int V, int K, int topk, float* hl, int32_t* ids, float* vals,
                    int32_t* root, cudaStream_t st) {
+  if (p.tc) {
+    // u for every row, then z = W2_k u_k on the tensor cores, then the top-k of z
+    for (int b0 = 0; b0 < B; b0 += p.bgroup) {
+      const int rc = launch_fc_nb(p, w, h, W1, b1, b0, std::min(p.bgroup, B - b0), H, K, st);
+      if (rc != MEDUSA_OK) return rc;
+    }
+    float* z = hl ? hl : w.z;
+    int rc = group_logits(p, w, h, W2, B, H, V, K, z, st);
+    if (rc != MEDUSA_OK) return rc;
+    for (int b0 = 0; b0 < B; b0 += p.bgroup) {
+      rc = launch_vocab_nb<T, true>(p, w, h, W2, lm, B, b0, std::min(p.bgroup, B - b0), H, V, K, topk, hl, ids, vals,
+                                    root, z, st);
+      if (rc != MEDUSA_OK) return rc;
+    }
+    return MEDUSA_OK;
+  }
   for (int b0 = 0; b0 < B; b0 += p.bgroup) {
     const int nb = std::min(p.bgroup, B - b0);
-    int rc;
-    if (nb == 1) rc = launch_heads<T, 1>(p, w, h, W1, b1, W2, lm, B, b0, nb, H, V, K, topk, hl, ids, vals, root, st);
-    else if (nb == 2) rc = launch_heads<T, 2>(p, w, h, W1, b1, W2, lm, B, b0, nb, H, V, K, topk, hl, ids, vals, root, st);
-    else if (nb <= 4) rc = launch_heads<T, 4>(p, w, h, W1, b1, W2, lm, B, b0, nb, H, V, K, topk, hl, ids, vals, root, st);
-    else if (nb <= 8) rc = launch_heads<T, 8>(p, w, h, W1, b1, W2, lm, B, b0, nb, H, V, K, topk, hl, ids, vals, root, st);
-    else rc = launch_heads<T, 16>(p, w, h, W1, b1, W2, lm, B, b0, nb, H, V, K, topk, hl, ids, vals, root, st);
+    int rc = launch_fc_nb(p, w, h, W1, b1, b0, nb, H, K, st);
+    if (rc == MEDUSA_OK)
+      rc = launch_vocab_nb<T, false>(p, w, h, W2, lm, B, b0, nb, H, V, K, topk, hl, ids, vals, root, nullptr, st);
     if (rc != MEDUSA_OK) return rc;
   }
   return MEDUSA_OK;
@@ -326,8 +396,8 @@ MEDUSA_API size_t medusa_heads_topk_workspace_size(int32_t B, int32_t H, int32_t
   if (B < 1 || H < 8 || V < 1 || K < 1 || topk < 1) return 0;
   const int es = dtype == MEDUSA_BF16 ? 2 : 4;
   HeadsPlan p;
-  if (!plan_heads(B, H, V, K, with_lm_head, es, topk, &p)) return 0;
-  return carve_heads_ws(nullptr, p, B, H, K, topk, es).bytes;
+  if (!plan_heads(B, H, V, K, with_lm_head, es, topk, true, &p)) return 0;
+  return carve_heads_ws(nullptr, p, B, H, V, K, topk, es).bytes;
 }
 
 MEDUSA_API int medusa_heads_topk(const void* h, const void* w1, const void* b1, const void* w2, const void* lm_head,
@@ -345,8 +415,8 @@ MEDUSA_API int medusa_heads_topk(const void* h, const void* w1, const void* b1, 
   if ((lm_head && !aligned16(lm_head)) || (head_logits && !aligned16(head_logits))) return MEDUSA_ERR_ALIGNMENT;
   const int es = dtype == MEDUSA_BF16 ? 2 : 4;
   HeadsPlan p;
-  if (!plan_heads(B, H, V, K, lm_head != nullptr, es, topk, &p)) return MEDUSA_ERR_UNSUPPORTED;
-  HeadsWs w = carve_heads_ws(ws, p, B, H, K, topk, es);
+  if (!plan_heads(B, H, V, K, lm_head != nullptr, es, topk, true, &p)) return MEDUSA_ERR_UNSUPPORTED;
+  HeadsWs w = carve_heads_ws(ws, p, B, H, V, K, topk, es);
   if (!ws || ws_bytes < w.bytes) return MEDUSA_ERR_WORKSPACE;
   auto st = reinterpret_cast<cudaStream_t>(stream);
   if (dtype == MEDUSA_BF16)
@@ -412,12 +482,12 @@ MEDUSA_API int medusa_heads_topk_noalloc(const void* h, const void* w1, const vo
   if ((lm_head && !aligned16(lm_head)) || (head_logits && !aligned16(head_logits))) return MEDUSA_ERR_ALIGNMENT;
   const int es = dtype == MEDUSA_BF16 ? 2 : 4;
   HeadsPlan p;
-  if (!plan_heads(B, H, V, K, lm_head != nullptr, es, topk, &p)) return MEDUSA_ERR_UNSUPPORTED;
-  if (carve_heads_ws(nullptr, p, B, H, K, topk, es).bytes > kNoAllocScratchBytes) return MEDUSA_ERR_SCRATCH_LIMIT;
+  if (!plan_heads(B, H, V, K, lm_head != nullptr, es, topk, false, &p)) return MEDUSA_ERR_UNSUPPORTED;
+  if (carve_heads_ws(nullptr, p, B, H, V, K, topk, es).bytes > kNoAllocScratchBytes) return MEDUSA_ERR_SCRATCH_LIMIT;
   void* scratch = nullptr;
   const int rc = heads_scratch_address(&scratch);
   if (rc != MEDUSA_OK) return rc;
-  HeadsWs w = carve_heads_ws(scratch, p, B, H, K, topk, es);
+  HeadsWs w = carve_heads_ws(scratch, p, B, H, V, K, topk, es);
   auto st = reinterpret_cast<cudaStream_t>(stream);
   // the ticket counters must start at zero whatever an earlier call left behind
   if (cudaMemsetAsync(w.counters, 0, static_cast<size_t>(p.nblk) * sizeof(int), st) != cudaSuccess) {

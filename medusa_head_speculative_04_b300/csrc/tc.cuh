@@ -259,4 +259,11 @@ bool make_tmap_bf16(CUtensorMap* m, const void* base, uint64_t rows, uint64_t co
 bool make_tmap_bf16_3d(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
                        uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t box1, uint32_t box2);
 
+// n_g row-major bf16 GEMMs on the persistent tcgen05 kernel of the verification
+// pass, fp32 results and no statistics: logits[r][g][v] = sum_i x[r][g][i] *
+// w[g*V + v][i] for r < R, g < n_g, v < V (x is [R][n_g][H], w is [n_g*V][H]).
+// Asynchronous on st; returns a MEDUSA_* status.
+int launch_group_logits_bf16(const void* x, int R, int n_g, const void* w, int H, int V, float* logits,
+                             cudaStream_t st);
+
 }  // namespace medusa

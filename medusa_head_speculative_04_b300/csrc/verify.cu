@@ -80,7 +80,7 @@ constexpr int F32_TILE = 256;  // vocabulary columns per statistics tile on the 
 
 struct VerifyPlan {
   int R, BN, n_mt, n_nt;
-  int qr, n_tiles, grid;  // bf16: rows per TMEM lane quadrant, tiles, persistent CTAs
+  int qr, n_g, n_tiles, grid;  // bf16: rows per TMEM lane quadrant, groups, tiles, persistent CTAs
   int n_parts;            // statistics partials per row (bf16, one row tile: one per CTA)
 };
 
@@ -91,36 +91,43 @@ struct VerifyPlan {
 // a little for the last tile's exposed epilogue.  At the 7B vocabulary that
 // is one 224-column tile per CTA.  With several row tiles the GEMM is
 // compute-bound and takes the widest MMA.
+// tcgen05 GEMM plan for R rows, n_g groups and V columns per group.
+VerifyPlan plan_tc(int R, int n_g, int V) {
+  VerifyPlan p{};
+  p.R = R;
+  const int sms = device_sm_count();
+  p.n_mt = cdiv(R, BM);
+  p.qr = cdiv(R, 4 * p.n_mt);
+  if (p.n_mt == 1) {
+    long best = -1;
+    for (int bn = 16; bn <= 256; bn += 16) {
+      const long per_cta = cdiv(n_g * cdiv(V, bn), sms);
+      const long cost = 8 * per_cta * (bn + 8 * p.qr) + bn;
+      if (best < 0 || cost <= best) {
+        best = cost;
+        p.BN = bn;
+      }
+    }
+  } else {
+    p.BN = 256;
+  }
+  p.n_nt = cdiv(V, p.BN);
+  p.n_g = n_g;
+  p.n_tiles = n_g * p.n_mt * p.n_nt;
+  p.grid = std::min(p.n_tiles, sms);
+  p.n_parts = p.n_mt == 1 ? p.grid : p.n_nt;
+  return p;
+}
+
 VerifyPlan plan_verify(int B, int T, int V, medusa_dtype dt) {
+  if (dt == MEDUSA_BF16) return plan_tc(B * T, 1, V);
   VerifyPlan p{};
   p.R = B * T;
-  if (dt == MEDUSA_BF16) {
-    const int sms = device_sm_count();
-    p.n_mt = cdiv(p.R, BM);
-    p.qr = cdiv(p.R, 4 * p.n_mt);
-    if (p.n_mt == 1) {
-      long best = -1;
-      for (int bn = 16; bn <= 256; bn += 16) {
-        const long per_cta = cdiv(cdiv(V, bn), sms);
-        const long cost = 8 * per_cta * (bn + 8 * p.qr) + bn;
-        if (best < 0 || cost <= best) {
-          best = cost;
-          p.BN = bn;
-        }
-      }
-    } else {
-      p.BN = 256;
-    }
-    p.n_nt = cdiv(V, p.BN);
-    p.n_tiles = p.n_mt * p.n_nt;
-    p.grid = std::min(p.n_tiles, sms);
-    p.n_parts = p.n_mt == 1 ? p.grid : p.n_nt;
-  } else {
-    p.n_mt = 1;
-    p.BN = F32_TILE;
-    p.n_nt = cdiv(V, F32_TILE);
-    p.n_parts = p.n_nt;
-  }
+  p.n_mt = 1;
+  p.n_g = 1;
+  p.BN = F32_TILE;
+  p.n_nt = cdiv(V, F32_TILE);
+  p.n_parts = p.n_nt;
   return p;
 }
 
@@ -161,9 +168,10 @@ struct EpiArgs {
   medusa_tree_dev tr;
   float inv_tau;  // 0 at temperature 0 (statistics beyond max/argmax skipped)
   float* logits;
-  float4* part;
+  float4* part;      // null: logits only (no statistics, no child gathers)
   float* child_z;
   int32_t* dev_status;
+  int n_g;           // GEMMs in the launch (group g: weight rows g*V.., activation group g)
 };
 
 // ------------------------------------------------------------------------
@@ -195,7 +203,9 @@ struct TcShape {
   int BN;       // vocabulary columns per tile
   int qr;       // tree rows per TMEM lane quadrant (a row tile holds 4*qr rows)
   int n_mt;     // row tiles
-  int n_tiles;  // n_mt * vocabulary tiles; tile t is row tile t % n_mt, vocabulary tile t / n_mt
+  int n_nt;     // vocabulary tiles per group
+  int n_g;      // groups (independent GEMMs sharing the launch)
+  int n_tiles;  // n_g * n_nt * n_mt; tile t is row tile t % n_mt, then vocabulary tile, then group
   int sw;       // lm_head ring stages
   int sx;       // X ring stages (<= kMaxStagesX)
 };
@@ -272,16 +282,16 @@ __device__ inline void block_stats(float (&v)[NCH * 16], int nv, int col0, float
 // One block of NCH 16-column chunks starting at chunk `ch` of the accumulator
 // at `tl`: load, statistics, logits copy and child gathers.
 template <int NCH>
-__device__ inline void epi_block(const EpiArgs& ea, uint32_t tl, int ch, int ncol, int n0, int r, int b, bool use,
-                                 float k2, bool tempered, int c_beg, uint64_t hits, float& m, int& arg, float& s,
-                                 float& w2, bool& nan_seen) {
+__device__ inline void epi_block(const EpiArgs& ea, uint32_t tl, int ch, int ncol, int n0, int r, int g, int b,
+                                 bool use, bool stats, float k2, bool tempered, int c_beg, uint64_t hits, float& m,
+                                 int& arg, float& s, float& w2, bool& nan_seen) {
   float v[NCH * 16];
   tc::tmem_ld16n<NCH>(tl + ch * 16, v);
   if (!use) return;
   const int c0 = ch * 16;
   const int nv = min(NCH * 16, ncol - c0);
   if (ea.logits && nv > 0) {
-    float* dst = ea.logits + static_cast<size_t>(r) * ea.V + n0 + c0;
+    float* dst = ea.logits + (static_cast<size_t>(r) * ea.n_g + g) * ea.V + n0 + c0;
 #pragma unroll
     for (int j = 0; j < NCH * 16; ++j)
       if (j < nv) dst[j] = v[j];
@@ -297,7 +307,7 @@ __device__ inline void epi_block(const EpiArgs& ea, uint32_t tl, int ch, int nco
       ea.child_z[static_cast<size_t>(b) * ea.T + c] = z;
     }
   }
-  block_stats<NCH>(v, nv, n0 + c0, k2, tempered, m, arg, s, w2, nan_seen);
+  if (stats) block_stats<NCH>(v, nv, n0 + c0, k2, tempered, m, arg, s, w2, nan_seen);
 }
 
 __device__ inline bool failed(const volatile int* f) { return *f != 0; }
@@ -331,7 +341,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) verify_tc_kernel(const __grid_c
   // different blocks, spreading the concurrent requests over more DRAM pages;
   // the compute-bound one keeps the CTAs that share a weight tile in step, so
   // the tile is still in L2 for all of them
-  const int rot = sh.n_mt == 1 ? static_cast<int>((static_cast<long>(blockIdx.x) * nk) / gridDim.x) : 0;
+  // (one GEMM only: the tiles of grouped GEMMs keep one summation order, so
+  // equal groups give bit-identical results)
+  const int rot = sh.n_mt == 1 && sh.n_g == 1 ? static_cast<int>((static_cast<long>(blockIdx.x) * nk) / gridDim.x) : 0;
 
   if (threadIdx.x == 0) {
     s_fail = 0;
@@ -364,12 +376,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) verify_tc_kernel(const __grid_c
       int i = 0;
       bool run = true;
       for (int t = blockIdx.x; t < sh.n_tiles && run; t += gridDim.x) {
-        const int n_t = t / sh.n_mt;
+        const int rest = t / sh.n_mt;
+        const int wrow = (rest / sh.n_nt) * ea.V + (rest % sh.n_nt) * BN;  // group g's rows start at g*V
         for (int k = 0; k < nk; ++k, ++i) {
           const int s = i % sh.sw;
           if (failed(&s_fail) || !tc::mbar_wait(wempty + s, ((i / sh.sw) & 1) ^ 1)) { s_fail = 1; run = false; break; }
           tc::mbar_expect_tx(wfull + s, W_BYTES);
-          tc::tma_load_2d(smem_u32(wsm + s * W_BYTES), &tma_w, ((k + rot) % nk) * BK, n_t * BN, wfull + s);
+          tc::tma_load_2d(smem_u32(wsm + s * W_BYTES), &tma_w, ((k + rot) % nk) * BK, wrow, wfull + s);
         }
       }
     }
@@ -381,13 +394,19 @@ __global__ void __launch_bounds__(kTcThreads, 1) verify_tc_kernel(const __grid_c
       bool run = true;
       for (int t = blockIdx.x; t < sh.n_tiles && run; t += gridDim.x) {
         const int row0 = (t % sh.n_mt) * 4 * qr;
+        const int g = t / sh.n_mt / sh.n_nt;
         for (int k = 0; k < nk; ++k, ++i) {
           const int s = i % sh.sx;
           if (failed(&s_fail) || !tc::mbar_wait(xempty + s, ((i / sh.sx) & 1) ^ 1)) { s_fail = 1; run = false; break; }
           tc::mbar_expect_tx(xfull + s, 4u * qr * BK * 2);
-          for (int q = 0; q < 4; ++q)
-            tc::tma_load_2d(smem_u32(xsm + s * kXStageBytes + q * 32 * BK * 2), &tma_x, ((k + rot) % nk) * BK, row0 + q * qr,
-                            xfull + s);
+          const int kx = ((k + rot) % nk) * BK;
+          for (int q = 0; q < 4; ++q) {
+            const uint32_t dst = smem_u32(xsm + s * kXStageBytes + q * 32 * BK * 2);
+            if (sh.n_g == 1)
+              tc::tma_load_2d(dst, &tma_x, kx, row0 + q * qr, xfull + s);
+            else  // [rows][groups][H]: box of qr rows of group g
+              tc::tma_load_3d(dst, &tma_x, kx, g, row0 + q * qr, xfull + s);
+          }
         }
       }
     }
@@ -429,6 +448,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) verify_tc_kernel(const __grid_c
     const int quad = warp & 3, grp = warp >> 2;
     const int ch0 = grp * NCH / kColGroups, ch1 = (grp + 1) * NCH / kColGroups;
     const bool tempered = ea.inv_tau > 0.f;
+    const bool stats = ea.part != nullptr;
     const float k2 = ea.inv_tau * kLog2e;
     int jl = 0;
     bool ok = true;
@@ -437,7 +457,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) verify_tc_kernel(const __grid_c
     bool run_nan = false;
     for (int t = blockIdx.x; t < sh.n_tiles; t += gridDim.x, ++jl) {
       const int a = jl & 1;
-      const int m_t = t % sh.n_mt, n_t = t / sh.n_mt;
+      const int m_t = t % sh.n_mt, n_t = (t / sh.n_mt) % sh.n_nt, g = t / sh.n_mt / sh.n_nt;
       const int r = m_t * 4 * qr + quad * qr + lane;
       const bool valid_row = lane < qr && r < ea.R;
       const uint32_t tl = taddr + (static_cast<uint32_t>(quad * 32) << 16) + a * ACC_STRIDE;
@@ -447,7 +467,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) verify_tc_kernel(const __grid_c
       // this group's columns (bit k: child c_beg + k; a node has < 64 children).
       int b = 0, c_beg = 0;
       uint64_t hits = 0;
-      if (valid_row) {
+      if (valid_row && stats) {
         b = r / ea.T;
         const int node = r % ea.T;
         c_beg = ea.tr.child_start[node];
@@ -472,10 +492,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) verify_tc_kernel(const __grid_c
         const bool use = valid_row;
         for (int ch = ch0; ch < ch1; ch += 4) {
           switch (min(4, ch1 - ch)) {
-            case 4: epi_block<4>(ea, tl, ch, ncol, n0, r, b, use, k2, tempered, c_beg, hits, m, arg, s, w2, nan_seen); break;
-            case 3: epi_block<3>(ea, tl, ch, ncol, n0, r, b, use, k2, tempered, c_beg, hits, m, arg, s, w2, nan_seen); break;
-            case 2: epi_block<2>(ea, tl, ch, ncol, n0, r, b, use, k2, tempered, c_beg, hits, m, arg, s, w2, nan_seen); break;
-            default: epi_block<1>(ea, tl, ch, ncol, n0, r, b, use, k2, tempered, c_beg, hits, m, arg, s, w2, nan_seen); break;
+            case 4: epi_block<4>(ea, tl, ch, ncol, n0, r, g, b, use, stats, k2, tempered, c_beg, hits, m, arg, s, w2, nan_seen); break;
+            case 3: epi_block<3>(ea, tl, ch, ncol, n0, r, g, b, use, stats, k2, tempered, c_beg, hits, m, arg, s, w2, nan_seen); break;
+            case 2: epi_block<2>(ea, tl, ch, ncol, n0, r, g, b, use, stats, k2, tempered, c_beg, hits, m, arg, s, w2, nan_seen); break;
+            default: epi_block<1>(ea, tl, ch, ncol, n0, r, g, b, use, stats, k2, tempered, c_beg, hits, m, arg, s, w2, nan_seen); break;
           }
         }
       }
@@ -483,6 +503,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) verify_tc_kernel(const __grid_c
       tc::fence_before_sync();
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(acc_empty + a);
+      if (!stats) continue;
       // groups 1.. hand their statistics to group 0, which merges them in
       // column order (ties keep the lower column) and writes the tile's partial
       float* xb = xh + a * (kColGroups - 1) * 5 * BM;
@@ -840,6 +861,8 @@ TcShape tc_shape(const VerifyPlan& p) {
   sh.BN = p.BN;
   sh.qr = p.qr;
   sh.n_mt = p.n_mt;
+  sh.n_nt = p.n_nt;
+  sh.n_g = p.n_g;
   sh.n_tiles = p.n_tiles;
   const size_t wb = static_cast<size_t>(p.BN) * BK * 2;
   // three X stages (L2 latency); the rest of shared memory goes to the weight
@@ -884,6 +907,24 @@ int dispatch_tc(const VerifyPlan& p, const CUtensorMap& mx, const CUtensorMap& m
 
 }  // namespace
 
+namespace medusa {
+
+int launch_group_logits_bf16(const void* x, int R, int n_g, const void* w, int H, int V, float* logits,
+                             cudaStream_t st) {
+  if (!x || !w || !logits || R < 1 || n_g < 1 || V < 1 || H < 8 || H % 8 != 0) return MEDUSA_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(w) || !aligned16(logits)) return MEDUSA_ERR_ALIGNMENT;
+  const VerifyPlan p = plan_tc(R, n_g, V);
+  CUtensorMap mx, mw;
+  const bool okx = n_g == 1 ? make_tmap_bf16(&mx, x, R, H, p.qr)
+                            : make_tmap_bf16_3d(&mx, x, H, n_g, R, static_cast<uint64_t>(H) * 2,
+                                                static_cast<uint64_t>(n_g) * H * 2, 1, p.qr);
+  if (!okx || !make_tmap_bf16(&mw, w, static_cast<uint64_t>(n_g) * V, H, p.BN)) return MEDUSA_ERR_CUDA;
+  const EpiArgs ea{R, V, 1, 0, nullptr, medusa_tree_dev{}, 0.f, logits, nullptr, nullptr, nullptr, n_g};
+  return dispatch_tc(p, mx, mw, H, ea, st);
+}
+
+}  // namespace medusa
+
 MEDUSA_API size_t medusa_verify_accept_workspace_size(const medusa_tree* tree, int32_t B, int32_t H, int32_t V,
                                                       medusa_dtype dtype) {
   if (!tree || B < 1 || H < 1 || V < 1) return 0;
@@ -916,7 +957,7 @@ MEDUSA_API int medusa_verify_accept(const medusa_tree* tree, const void* x, cons
   if (!ws || ws_bytes < w.bytes) return MEDUSA_ERR_WORKSPACE;
   auto st = reinterpret_cast<cudaStream_t>(stream);
   const float inv_tau = temperature > 0.f ? 1.f / temperature : 0.f;
-  EpiArgs ea{p.R, V, T, p.n_parts, tree_tokens, tree->dev, inv_tau, logits, w.part, w.child_z, dev_status};
+  EpiArgs ea{p.R, V, T, p.n_parts, tree_tokens, tree->dev, inv_tau, logits, w.part, w.child_z, dev_status, 1};
 
   if (dtype == MEDUSA_BF16) {
     CUtensorMap mx, mw;

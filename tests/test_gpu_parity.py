@@ -161,6 +161,22 @@ SMALL_BF16_D64 = dataclasses.replace(SMALL_BF16, name="small_bf16_d64", config_i
 SMALL_BF16_G3 = dataclasses.replace(SMALL_BF16, name="small_bf16_g3", config_id=13, Hq=6, Hkv=2)
 
 
+def test_zero_init_heads_bitwise_tensor_core_path(mb):
+    """The same example at three batch rows with the root given, where z_k = W2_k u_k runs
+    as one grouped tcgen05 GEMM: every head's logits are still bitwise identical."""
+    wl = SMALL_BF16
+    inp = synth.make_inputs(wl, "cuda", variant="zeroinit")
+    step = make_step(mb, wl, inp)
+    step.heads(inp.h, inp.W1, inp.b1, inp.W2)
+    torch.cuda.synchronize()
+    hl = step.head_logits
+    for k in range(1, wl.K):
+        assert torch.equal(hl[:, k], hl[:, 0])
+        assert torch.equal(step.topk_ids[:, k], step.topk_ids[:, 0])
+    o = step_oracle_inputs(inp)
+    assert rel_err(hl[:, 0], o["h"] @ o["lm_head"].T) < TOL[wl.dtype]
+
+
 @pytest.mark.parametrize("wl", [SMALL_BF16, SMALL_BF16_D64, SMALL_BF16_G3], ids=lambda w: w.name)
 @pytest.mark.parametrize("temperature", [0.0, 0.7])
 @pytest.mark.parametrize("variant", ["random", "plant"])
