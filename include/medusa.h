@@ -135,6 +135,9 @@ void medusa_tree_destroy(medusa_tree* tree);
  *     not touched (it then holds the previous step's next_root).
  *   For bf16 data u is rounded to bf16 before W2 (the W2 stream is bf16).
  *   Limits: 1 <= B <= MEDUSA_MAX_BATCH, H % 8 == 0, 1 <= topk <= min(V, MEDUSA_MAX_TOPK).
+ *   bf16 with B >= 3 and lm_head == NULL runs W1 h and W2_k u_k on the tensor
+ *   cores; the workspace then also holds [B,K,V] and [B,K*H] fp32 buffers
+ *   (medusa_heads_topk_workspace_size includes them).
  * ---------------------------------------------------------------------- */
 size_t medusa_heads_topk_workspace_size(int32_t B, int32_t H, int32_t V, int32_t K, int32_t topk,
                                         int32_t with_lm_head, medusa_dtype dtype);

@@ -110,7 +110,8 @@ bool plan_heads(int B, int H, int V, int K, int with_root, int esize, int topk, 
 
 struct HeadsWs {
   void* u;
-  float* z;  // [B, K, V] logits of the tensor-core path when the caller keeps none
+  float* z;    // [B, K, V] logits of the tensor-core path when the caller keeps none
+  float* zfc;  // [B, K*H] W1_k h of the tensor-core path
   float* cand_v;
   int* cand_i;
   int* counters;
@@ -125,9 +126,11 @@ HeadsWs carve_heads_ws(void* base, const HeadsPlan& p, int B, int H, int V, int 
   size_t ncand = static_cast<size_t>(p.nblk) * B * p.cph * topk;
   size_t ov = take(ncand * 4), oi = take(ncand * 4), oc = take(static_cast<size_t>(p.nblk) * 4);
   size_t oz = p.tc ? take(static_cast<size_t>(B) * K * V * 4) : 0;
+  size_t ozf = p.tc ? take(static_cast<size_t>(B) * K * H * 4) : 0;
   char* c = static_cast<char*>(base);
   w.u = c ? c + ou : nullptr;
   w.z = c && p.tc ? reinterpret_cast<float*>(c + oz) : nullptr;
+  w.zfc = c && p.tc ? reinterpret_cast<float*>(c + ozf) : nullptr;
   w.cand_v = c ? reinterpret_cast<float*>(c + ov) : nullptr;
   w.cand_i = c ? reinterpret_cast<int*>(c + oi) : nullptr;
   w.counters = c ? reinterpret_cast<int*>(c + oc) : nullptr;
@@ -187,6 +190,25 @@ __global__ void __launch_bounds__(kThreads) heads_fc_kernel(const T* __restrict_
         }
       }
     }
+  }
+}
+
+// K1 on the tensor-core path: u = h + SiLU(zfc + b1) for zfc = W1_k h from the
+// GEMM, elementwise over [B, K*H] (the same arithmetic as heads_fc_kernel's
+// epilogue).
+template <typename T>
+__global__ void __launch_bounds__(kThreads) heads_fc_act_kernel(const T* __restrict__ h, const T* __restrict__ b1,
+                                                                const float* __restrict__ zfc, int B, int K, int H,
+                                                                T* __restrict__ u) {
+  pdl_wait();
+  pdl_trigger();
+  const long kh = static_cast<long>(K) * H, n = static_cast<long>(B) * kh;
+  for (long e = blockIdx.x * static_cast<long>(blockDim.x) + threadIdx.x; e < n;
+       e += static_cast<long>(gridDim.x) * blockDim.x) {
+    const long b = e / kh, row = e % kh;
+    const float a = zfc[e] + Elem<T>::to_f(b1[row]);
+    const float silu = a / (1.0f + expf(-a));  // SiLU(a) = a * sigmoid(a)
+    u[e] = Elem<T>::from_f(Elem<T>::to_f(h[b * H + row % H]) + silu);
   }
 }
 
@@ -350,12 +372,25 @@ int launch_fc_nb(const HeadsPlan& p, const HeadsWs& w, const T* h, const T* W1, 
   return launch_fc<T, 16>(p, w, h, W1, b1, b0, nb, H, K, st);
 }
 
-int group_logits(const HeadsPlan&, const HeadsWs&, const float*, const float*, int, int, int, int, float*,
-                 cudaStream_t) {
-  return MEDUSA_ERR_UNSUPPORTED;  // the tensor-core path is bf16 only
+// The tensor-core path (bf16 only): u = h + SiLU(W1_k h + b1_k) with W1 as one
+// [K*H, H] GEMM plus an elementwise launch, then z_k = W2_k u_k as K grouped GEMMs.
+int tc_heads(const HeadsWs&, const float*, const float*, const float*, const float*, int, int, int, int, float*,
+             cudaStream_t) {
+  return MEDUSA_ERR_UNSUPPORTED;
 }
-int group_logits(const HeadsPlan&, const HeadsWs& w, const __nv_bfloat16*, const __nv_bfloat16* W2, int B, int H,
-                 int V, int K, float* z, cudaStream_t st) {
+int tc_heads(const HeadsWs& w, const __nv_bfloat16* h, const __nv_bfloat16* W1, const __nv_bfloat16* b1,
+             const __nv_bfloat16* W2, int B, int H, int V, int K, float* z, cudaStream_t st) {
+  int rc = launch_group_logits_bf16(h, B, 1, W1, H, K * H, w.zfc, st);
+  if (rc != MEDUSA_OK) return rc;
+  const long n = static_cast<long>(B) * K * H;
+  const int blocks = static_cast<int>(std::min<long>(cdiv(static_cast<int>(std::min<long>(n, 1L << 30)), kThreads),
+                                                     4L * device_sm_count()));
+  if (launch_pdl(heads_fc_act_kernel<__nv_bfloat16>, dim3(blocks), dim3(kThreads), 0, st, h, b1,
+                 static_cast<const float*>(w.zfc), B, K, H, static_cast<__nv_bfloat16*>(w.u)) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return MEDUSA_ERR_CUDA;
+  }
+  MEDUSA_LAUNCH_CHECK();
   return launch_group_logits_bf16(w.u, B, K, W2, H, V, z, st);
 }
 
@@ -364,13 +399,9 @@ int heads_dispatch(const HeadsPlan& p, const HeadsWs& w, const T* h, const T* W1
                    const T* lm, int B, int H, int V, int K, int topk, float* hl, int32_t* ids, float* vals,
                    int32_t* root, cudaStream_t st) {
   if (p.tc) {
-    // u for every row, then z = W2_k u_k on the tensor cores, then the top-k of z
-    for (int b0 = 0; b0 < B; b0 += p.bgroup) {
-      const int rc = launch_fc_nb(p, w, h, W1, b1, b0, std::min(p.bgroup, B - b0), H, K, st);
-      if (rc != MEDUSA_OK) return rc;
-    }
+    // u and z = W2_k u_k on the tensor cores, then the top-k of z
     float* z = hl ? hl : w.z;
-    int rc = group_logits(p, w, h, W2, B, H, V, K, z, st);
+    int rc = tc_heads(w, h, W1, b1, W2, B, H, V, K, z, st);
     if (rc != MEDUSA_OK) return rc;
     for (int b0 = 0; b0 < B; b0 += p.bgroup) {
       rc = launch_vocab_nb<T, true>(p, w, h, W2, lm, B, b0, std::min(p.bgroup, B - b0), H, V, K, topk, hl, ids, vals,
