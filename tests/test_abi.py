@@ -98,3 +98,17 @@ def test_binding_has_no_cpu_path():
         if f.endswith(".py"):
             s = open(os.path.join(ROOT, "medusa_head_speculative_04_b300", f)).read()
             assert "oracle" not in s.replace("oracle-free", ""), f
+
+
+def test_heads_workspace_holds_the_tensor_core_buffers(lib):
+    """bf16 with three or more batch rows and the root given takes the tensor-core heads
+    path, whose workspace also holds the [B,K,V] logits and the [B,K*H] W1 h buffers; the
+    lm_head-root variant and fp32 stay on the CUDA-core path without them."""
+    f = lib.lib.medusa_heads_topk_workspace_size
+    B, H, V, K, topk = 3, 4096, 32000, 5, 10
+    extra = B * K * V * 4 + B * K * H * 4
+    tc = f(B, H, V, K, topk, 0, 1)
+    assert tc >= extra
+    assert 0 < f(B, H, V, K, topk, 1, 1) < extra
+    assert 0 < f(B, H, V, K, topk, 0, 0) < extra
+    assert 0 < f(2, H, V, K, topk, 0, 1) < extra
