@@ -278,13 +278,12 @@ __global__ void __launch_bounds__(kThreads) heads_vocab_kernel(
   }
   __syncthreads();
 
-  // local top-k of this slice, per batch row
-  for (int b = 0; b < nb; ++b) {
-    float* outv = cand_v + ((static_cast<size_t>(blk) * B + b0 + b) * cph + cta) * topk;
-    int* outi = cand_i + ((static_cast<size_t>(blk) * B + b0 + b) * cph + cta) * topk;
-    block_topk(zs + static_cast<size_t>(b) * rpc, nullptr, v0, n, kk, fv, fi, sv, si);
-    for (int t = threadIdx.x; t < kk; t += blockDim.x) { outv[t] = fv[t]; outi[t] = fi[t]; }
-    __syncthreads();
+  // local top-k of this slice: one warp per batch row, rows side by side (a
+  // block-wide selection per row would serialise the rows behind its barriers)
+  for (int b = warp; b < nb; b += kWarps) {
+    const size_t cb = ((static_cast<size_t>(blk) * B + b0 + b) * cph + cta) * topk;
+    warp_topk_slice(zs + static_cast<size_t>(b) * rpc, nullptr, v0, n, kk, cand_v + cb, cand_i + cb,
+                    __int_as_float(0x7fc00000));
   }
 
   // the last CTA of this block merges every slice's candidates
