@@ -65,3 +65,21 @@ def test_reference_arm_under_torchrun_prints_one_line():
     assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["unit"] == "verifies/s"
     assert d["value"] > 0 and d["cpu_baseline"]["kind"] == "oracle"
     assert d["e2e"] == {"value": d["value"], "unit": "verifies/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+
+
+def test_tree_option_builds_the_requested_trees():
+    import argparse
+
+    import bench
+    a = argparse.Namespace(workload="vicuna7b", tree=None)
+    assert len(bench.select_workload(a).choices()) == 64
+    for spec, T in (("cartesian:2,3", 9), ("seeded:256", 257), ("cartesian:10,10,10", 1111)):
+        a.tree = spec
+        wl = bench.select_workload(a)
+        assert len(wl.choices()) + 1 == T and wl.name.endswith(spec)
+    a.tree = "cartesian:2,2,2,2,2,2"   # deeper than the workload's 5 heads
+    try:
+        bench.select_workload(a)
+        raise AssertionError("a tree deeper than the heads was accepted")
+    except SystemExit:
+        pass
