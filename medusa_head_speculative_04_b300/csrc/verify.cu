@@ -12,15 +12,18 @@
 // posterior_alpha) -> best_candidate, accept_length.
 //
 // K5 (bf16): logits = X lm_head^T for every tree node is a GEMM with M = tree
-// rows (B*T) and N = vocabulary.  tcgen05.mma accumulates a 128 x BN tile in
-// TMEM from TMA-fed, 128-byte-swizzled shared-memory stages (one producer
-// thread, one MMA thread).  The epilogue (4 warps, one TMEM lane = one tree
-// node each) never writes the logits unless asked: it reduces its vocabulary
-// tile to (max, argmax, sum of exp, sum of exp * logit) at the temperature and
-// picks out the logits of the node's children tokens.
+// rows (B*T) and N = vocabulary.  A persistent kernel: tcgen05.mma accumulates
+// 128 x BN tiles in two alternating TMEM accumulators from TMA-fed,
+// 128-byte-swizzled shared-memory rings (one producer thread per operand, one
+// MMA thread).  The epilogue (eight warps, one TMEM lane = one tree node) never
+// writes the logits unless asked: it reduces its vocabulary tile to (max,
+// argmax, sum of exp, sum of exp * logit) at the temperature and picks out the
+// logits of the node's children tokens.  The same kernel, with a logits-only
+// epilogue and several GEMMs per launch, serves the Medusa heads at larger
+// batches (launch_group_logits_bf16).
 // K5 (fp32): CUDA-core GEMV into a logits buffer, then the same statistics.
-// K6a merges the per-tile statistics of every node; K6b decides acceptance,
-// the longest kept prefix, the next root, one CTA per request.
+// K6 merges the statistics of every node and tests its children; the last CTA
+// of a request then picks the longest kept prefix and the next root.
 #include <algorithm>
 #include <mutex>
 
