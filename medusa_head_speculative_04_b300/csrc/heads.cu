@@ -11,6 +11,8 @@
 // the dot products run on CUDA cores from a shared-memory copy of the
 // activations).  K2 fuses the top-k: every CTA keeps the top-k of its slice of
 // the vocabulary, and the last CTA of a head (ticket counter) merges them.
+// From kTcMinRows batch rows both products run on the tcgen05 GEMM of the
+// verification pass instead, and K2 only selects from the logits it wrote.
 #include <algorithm>
 #include <mutex>
 
