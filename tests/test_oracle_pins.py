@@ -315,6 +315,14 @@ def test_longest_prefix_and_tie_break():
     assert acc["accept_len"][0] == 0 and acc["best_node"][0] == 0
     assert acc["accepted_tokens"][0].tolist() == [0, -1, -1]
     assert acc["next_root"][0] == 29                     # greedy token of the winner (the root)
+    assert acc["best_path"][0] == 0                      # every path runs through the root
+    # (b') an inner winner: node 2 passes, none of its children does -> the first path through
+    #      it is the one ending at its first child, node 6 (path index 3)
+    z = _tree_logits(tt, tokens, V, [2])
+    z[0, 2, 29] = 10.0
+    acc = oracle.typical_accept(z, tokens, tt, 0.0, 0.09, 0.3)
+    assert acc["best_node"][0] == 2 and acc["accept_len"][0] == 1 and acc["best_path"][0] == 3
+    assert acc["accepted_tokens"][0].tolist() == [0, 12, -1] and acc["next_root"][0] == 29
     # (c) temperature > 0 with one clear branch
     z = _tree_logits(tt, tokens, V, [2, 8])
     acc = oracle.typical_accept(z * 3, tokens, tt, 0.7, 0.09, 0.3)
