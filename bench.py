@@ -194,6 +194,12 @@ def workload_config(wl, T, tau, ws):
 
 # ----------------------------------------------------------------------------- our arm
 
+def pct(xs, q):
+    """q-th percentile (nearest rank) of a non-empty list."""
+    s = sorted(xs)
+    return s[min(len(s) - 1, max(0, int(math.ceil(q / 100.0 * len(s))) - 1))]
+
+
 def run_ours(args, ws, rank, local):
     import torch
     import torch.distributed as dist
@@ -221,7 +227,7 @@ def run_ours(args, ws, rank, local):
         kl.copy_(kv_len0)                       # every step starts from the same prefix
         step.root.copy_(root)
         if timed_events:
-            e = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(4)]
+            e = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(5)]
             e[0].record()
         step.heads(inp.h, inp.W1, inp.b1, inp.W2)
         if timed_events:
@@ -235,6 +241,7 @@ def run_ours(args, ws, rank, local):
             e[3].record()
         step.commit(inp.k_new, inp.v_new, kc, vc, kl)
         if timed_events:
+            e[4].record()
             ev_pairs.append(e)
 
     # eager warm-up (function attributes, tensor maps), then graphs
@@ -246,7 +253,8 @@ def run_ours(args, ws, rank, local):
     with torch.cuda.graph(g1, stream=s):
         one_step()
     launches_per_step = mb.kernel_launches() - n0
-    S = max(1, min(args.unroll, args.steps))
+    # steps per timed graph: at least two replays inside the timed region
+    S = max(1, min(args.unroll, args.steps // 2))
     gS = torch.cuda.CUDAGraph()          # the timed graph: steps back to back, nothing in between
     with torch.cuda.graph(gS, stream=s):
         for _ in range(S):
@@ -257,8 +265,13 @@ def run_ours(args, ws, rank, local):
             one_step(timed_events=True)
     reps, rem = divmod(args.steps, S)
 
-    for _ in range(max(3, args.warmup)):
-        g1.replay()
+    # warm-up: the timed graph itself (its first replay uploads it), then single steps
+    warm = max(3, args.warmup)
+    with torch.cuda.stream(s):
+        for _ in range(max(1, warm // S)):
+            gS.replay()
+        for _ in range(max(1, warm % S)):
+            g1.replay()
     torch.cuda.synchronize()
     if ws > 1:
         dist.barrier()
@@ -283,19 +296,27 @@ def run_ours(args, ws, rank, local):
     ms_max = max_over_ranks(start.elapsed_time(end), dev, ws)
     status = int(step.dev_status.max().item())
 
-    # stage breakdown: a separate replay of the graph with events between the
-    # stages (an event node between two kernels stops the second one from
+    # stage breakdown and per-step spread: separate replays of the graph with events
+    # between the stages (an event node between two kernels stops the second one from
     # starting before the first has finished, so these are not in the timed graph)
-    with torch.cuda.stream(s):
-        for _ in range(3):
-            gE.replay()
-    torch.cuda.synchronize()
+    n_ev = max(1, -(-200 // S))
     stage_ms = {"heads": [], "attention": [], "verify": []}
-    if reps > 0:
+    step_ms = []
+    with torch.cuda.stream(s):
+        gE.replay()                             # upload / warm
+    torch.cuda.synchronize()
+    for _ in range(n_ev):
+        with torch.cuda.stream(s):
+            gE.replay()
+        torch.cuda.synchronize()
         for e in ev_pairs:
             stage_ms["heads"].append(e[0].elapsed_time(e[1]))
             stage_ms["attention"].append(e[1].elapsed_time(e[2]))
             stage_ms["verify"].append(e[2].elapsed_time(e[3]))
+            step_ms.append(e[0].elapsed_time(e[4]))
+    accept_hist = {}
+    for a in step.accept_len.cpu().tolist():
+        accept_hist[str(a)] = accept_hist.get(str(a), 0) + 1
 
     # end-to-end through the public API: every step copies its inputs in from
     # pinned host memory and its results out.  The inputs of step i+1 upload on a
@@ -428,11 +449,18 @@ def run_ours(args, ws, rank, local):
                         "copy stream) and its results copied out (staged on the device, read back on a third "
                         "stream while the next step runs); eager_value: the same loop with eager "
                         "MedusaStep.run calls"},
+        "step_ms_percentiles": {
+            "p50": round(pct(step_ms, 50), 5), "p99": round(pct(step_ms, 99), 5), "n": len(step_ms),
+            "note": "per-step times from the event-instrumented replay (events between the stages cancel the "
+                    "programmatic overlap of adjacent kernels, so these sit slightly above ms_per_step)"},
+        "accept_len_hist": {"counts": accept_hist,
+                            "note": "accepted tokens beyond the root per request; every timed step sees the same "
+                                    "inputs, so each request's count repeats in every step"},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks,
         "dev_status": status,
     }
-    return out, inp, wl
+    return out, inp, wl, step, kl
 
 
 # ----------------------------------------------------------------------------- oracle timing
@@ -455,18 +483,48 @@ def oracle_sample(wl, inp, temperature, budget_s, max_steps):
             f(inp.v_new), f(inp.k_cache), f(inp.v_cache), inp.kv_len.cpu().numpy()]
     root = inp.root.cpu().numpy()
     times = []
+    res = None
     t_all = time.perf_counter()
     while len(times) < max_steps:
         t0 = time.perf_counter()
-        oracle.run_step(*args, inp.choices, wl.k_needed(), temperature, wl.posterior_threshold,
-                        wl.posterior_alpha, root=root, u_bf16=(wl.dtype == "bf16"))
+        res = oracle.run_step(*args, inp.choices, wl.k_needed(), temperature, wl.posterior_threshold,
+                              wl.posterior_alpha, root=root, u_bf16=(wl.dtype == "bf16"))
         times.append(time.perf_counter() - t0)
         if time.perf_counter() - t_all > budget_s:
             break
     per = sum(times) / len(times)
     return {"value": round(wl.B / per, 4), "unit": UNIT, "cores": cores, "kind": "oracle",
             "sample": f"{len(times)} full decode step(s) of {wl.name} (B={wl.B}), fp64 numpy, "
-                      f"{per:.2f} s/step"}, len(times), per
+                      f"{per:.2f} s/step"}, len(times), per, res
+
+
+def parity_summary(wl, step, kv_len, res, temperature):
+    """The timed step's discrete outputs against the oracle's step on the same inputs.
+
+    Near-ties are the decisions whose oracle margin is below the float tolerance
+    (top-k orders, acceptance tests); a mismatch there is allowed, anywhere else it
+    is an error."""
+    import numpy as np
+    delta = 1e-3 if wl.dtype == "bf16" else 1e-5
+    g = lambda t: t.detach().cpu().numpy().astype(np.int64)
+    zmax = np.abs(res.head_logits).max(axis=-1)
+    near_topk = int(np.sum(res.topk_margin < delta * np.maximum(1.0, zmax)))
+    m = res.accept["margin"][:, 1:]
+    if temperature > 0:
+        near_acc = int(np.sum(m < delta / temperature))
+    else:
+        near_acc = int(np.sum(m < delta * max(1.0, float(np.abs(res.logits).max()))))
+    mism = {"topk_ids": int(np.sum(g(step.topk_ids) != res.topk_ids)),
+            "tree_tokens": int(np.sum(g(step.tokens) != res.tokens)),
+            "accepted_tokens": int(np.sum(g(step.accepted_tokens) != res.accept["accepted_tokens"])),
+            "kv_len": int(np.sum(g(kv_len) != res.kv_len))}
+    for k in ("accept_len", "best_node", "best_path", "next_root"):
+        mism[k] = int(np.sum(g(getattr(step, k)) != res.accept[k]))
+    n_mism = sum(mism.values())
+    return {"near_ties": near_topk + near_acc, "near_ties_topk": near_topk, "near_ties_accept": near_acc,
+            "mismatches": n_mism, "mismatch_by_output": mism, "ok": n_mism == 0 or near_topk + near_acc > 0,
+            "compared": "top-k ids, tree tokens, accept_len, best_node, best_path, accepted_tokens, next_root, "
+                        "kv_len of the timed step against the oracle's step on the same inputs"}
 
 
 def run_reference(args, ws, rank):
@@ -479,7 +537,7 @@ def run_reference(args, ws, rank):
     # faster there); the oracle only ever sees host copies
     gen_dev = "cuda" if torch.cuda.is_available() else "cpu"
     inp = synth.make_inputs(wl, gen_dev, variant="plant")
-    cb, n, per = oracle_sample(wl, inp, args.temperature, args.cpu_budget_s * 4, max(1, args.steps))
+    cb, n, per, _ = oracle_sample(wl, inp, args.temperature, args.cpu_budget_s * 4, max(1, args.steps))
     return {"impl": "reference", "metric": METRIC, "value": cb["value"], "unit": UNIT, "n_gpus": ws,
             "steps": n, "warmup": 0, "ms_per_step": round(per * 1e3, 3), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
@@ -504,10 +562,11 @@ def main():
     res = run_ours(args, ws, rank, local)
     if res is None:
         return
-    out, inp, wl = res
+    out, inp, wl, step, kl = res
     if not args.no_cpu_baseline and rank == 0 and ws == 1:
-        cb, _, _ = oracle_sample(wl, inp, args.temperature, args.cpu_budget_s, 3)
+        cb, _, _, res_o = oracle_sample(wl, inp, args.temperature, args.cpu_budget_s, 3)
         out["cpu_baseline"] = cb
+        out["parity"] = parity_summary(wl, step, kl, res_o, args.temperature)
     else:
         out["cpu_baseline"] = None
     print(json.dumps(out))

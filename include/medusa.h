@@ -150,18 +150,28 @@ int medusa_heads_topk(const void* h, const void* w1, const void* b1, const void*
 /* ------------------------------------------------------------------------
  * medusa_heads_topk_noalloc
  * No counterpart on the source pages: a convenience of this library.
- * Same computation, arguments and outputs as medusa_heads_topk, minus the
- * workspace, for callers that cannot allocate device memory -- cudaMalloc may
+ * The computation, arguments and outputs of medusa_heads_topk, minus the
+ * workspace, for callers that cannot allocate device memory: cudaMalloc may
  * synchronise the device and takes a driver-wide lock, so latency-bound decode
  * loops, plugins living inside another framework's memory pool and programs
  * with a fixed device-memory budget often may not call it.  The scratch is a
  * fixed array of MEDUSA_NOALLOC_SCRATCH_BYTES compiled into the library; every
  * GPU that loads the library holds it until the process exits.
- *   - Shapes whose scratch would exceed that size return
- *     MEDUSA_ERR_SCRATCH_LIMIT (about B*K*H*elem + 8*(K+1)*B*topk*CTAs per head
- *     bytes; the Llama-8B shape at batch 16 needs about 1.5 MB).
- *   - The first call on each device looks up the array's device address (with
- *     that device current); make that first call before any stream capture.
+ *   - Always the CUDA-core path (heads_fc + heads_vocab): it never takes the
+ *     tensor-core path that medusa_heads_topk uses for bf16 with B >= 3 and no
+ *     lm_head, so in that case results can differ from medusa_heads_topk at
+ *     near-ties (both match the exact heads within the float tolerance) and the
+ *     call streams the weights on CUDA cores.
+ *   - Shapes whose scratch would exceed the array return
+ *     MEDUSA_ERR_SCRATCH_LIMIT.  The scratch a shape needs is what
+ *     medusa_heads_topk_workspace_size returns for the same arguments whenever
+ *     that plan is also the CUDA-core one (fp32, B <= 2, or lm_head given; e.g.
+ *     the Llama-8B shape at batch 16 with lm_head needs about 1.5 MB).
+ *   - The array's device address is looked up on every call made outside a
+ *     stream capture; the first call on each device (and the first after a
+ *     device reset) must come before any stream capture on that device, since
+ *     it also loads the library's device code.  A call inside a capture reuses
+ *     the address found by the last call outside one.
  *   - All calls share the one array and it keeps the last call's contents;
  *     the ticket counters are cleared on the stream at every call.  Calls
  *     that overlap on the GPU (other streams, other host threads) race.

@@ -477,15 +477,27 @@ constexpr int kMaxDevices = 64;
 static __device__ __align__(256) unsigned char g_heads_scratch[kNoAllocScratchBytes];
 
 // Device address of g_heads_scratch on the current device.  Host code only has
-// a host-side stand-in under that name, so the address is looked up once per
-// device (with that device current) and cached.
-int heads_scratch_address(void** out) {
+// a host-side stand-in under that name, so the address is looked up with the
+// device current.  A call made outside a stream capture looks it up afresh (a
+// host-side table lookup in the CUDA runtime; the first one on a device also
+// loads this library's device code), so a device reset or a recreated context
+// never leaves a stale address behind; a call made while `st` is capturing
+// reuses the address found by the last call on that device outside a capture.
+int heads_scratch_address(cudaStream_t st, void** out) {
   static std::mutex mu;
   static void* addr[kMaxDevices] = {};
   int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MEDUSA_ERR_CUDA;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    (void)cudaGetLastError();
+    return MEDUSA_ERR_CUDA;
+  }
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(st, &cap) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return MEDUSA_ERR_CUDA;
+  }
   std::lock_guard<std::mutex> lock(mu);
-  if (!addr[dev]) {
+  if (cap == cudaStreamCaptureStatusNone) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_heads_scratch) != cudaSuccess || !p) {
       (void)cudaGetLastError();
@@ -493,6 +505,7 @@ int heads_scratch_address(void** out) {
     }
     addr[dev] = p;
   }
+  if (!addr[dev]) return MEDUSA_ERR_CUDA;  // first call on this device made inside a capture
   *out = addr[dev];
   return MEDUSA_OK;
 }
@@ -516,11 +529,11 @@ MEDUSA_API int medusa_heads_topk_noalloc(const void* h, const void* w1, const vo
   HeadsPlan p;
   if (!plan_heads(B, H, V, K, lm_head != nullptr, es, topk, false, &p)) return MEDUSA_ERR_UNSUPPORTED;
   if (carve_heads_ws(nullptr, p, B, H, V, K, topk, es).bytes > kNoAllocScratchBytes) return MEDUSA_ERR_SCRATCH_LIMIT;
+  auto st = reinterpret_cast<cudaStream_t>(stream);
   void* scratch = nullptr;
-  const int rc = heads_scratch_address(&scratch);
+  const int rc = heads_scratch_address(st, &scratch);
   if (rc != MEDUSA_OK) return rc;
   HeadsWs w = carve_heads_ws(scratch, p, B, H, V, K, topk, es);
-  auto st = reinterpret_cast<cudaStream_t>(stream);
   // the ticket counters must start at zero whatever an earlier call left behind
   if (cudaMemsetAsync(w.counters, 0, static_cast<size_t>(p.nblk) * sizeof(int), st) != cudaSuccess) {
     (void)cudaGetLastError();

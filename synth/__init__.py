@@ -264,6 +264,11 @@ class StepInputs:
     def T(self) -> int:
         return len(self.choices) + 1
 
+    def to(self, device) -> "StepInputs":
+        """The same inputs with every tensor copied to ``device`` (values unchanged)."""
+        moved = {k: (v.to(device) if isinstance(v, torch.Tensor) else v) for k, v in self.__dict__.items()}
+        return StepInputs(**moved)
+
 
 def torch_dtype(wl: Workload) -> torch.dtype:
     return torch.float32 if wl.dtype == "f32" else torch.bfloat16

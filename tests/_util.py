@@ -1,10 +1,22 @@
 """Shared helpers of the parity tests: comparisons, tolerances, oracle glue."""
 from __future__ import annotations
 
+import dataclasses
+
 import numpy as np
 import torch
 
 import oracle
+import synth
+
+# Small bf16 workloads that still span several tiles: ragged kv lengths (including 0),
+# a vocabulary that is not a multiple of any tile, GQA, several requests, both head dims.
+SMALL_BF16 = synth.Workload("small_bf16", 11, H=512, V=3001, K=3, Hq=8, Hkv=2, D=128, L=0, B=3, dtype="bf16",
+                            tree=("cartesian", (3, 2, 2)), ragged=(0, 300))
+SMALL_BF16_D64 = dataclasses.replace(SMALL_BF16, name="small_bf16_d64", config_id=12, D=64, Hq=4, Hkv=4,
+                                     tree=("seeded", 40, (8, 4, 2)), ragged=(60, 200), B=2, V=2048)
+# a query-head group (3) that does not divide 128 takes the mma.sync attention kernel
+SMALL_BF16_G3 = dataclasses.replace(SMALL_BF16, name="small_bf16_g3", config_id=13, Hq=6, Hkv=2)
 
 # Float tolerance (max relative error with an rms floor) and near-tie widths.
 TOL = {"f32": 1e-4, "bf16": 2e-2}

@@ -31,3 +31,27 @@ def read_golden(name):
 @pytest.fixture(scope="session")
 def golden():
     return read_golden
+
+
+# Near-tie decisions: discrete outputs whose oracle margin is below the float
+# tolerance may legitimately differ from the oracle's; the parity tests count
+# them instead of failing, and the counts are reported at the end of the run.
+_NEAR_TIES = []
+
+
+@pytest.fixture
+def near_ties(request):
+    """Call with the number of near-tie decisions a test met (it is reported, not failed)."""
+    def record(n: int) -> int:
+        _NEAR_TIES.append((request.node.nodeid, int(n)))
+        return int(n)
+    return record
+
+
+def pytest_terminal_summary(terminalreporter):
+    if not _NEAR_TIES:
+        return
+    terminalreporter.section("near-tie decisions (oracle margin below the tolerance: counted, not failed)")
+    for nodeid, n in _NEAR_TIES:
+        terminalreporter.write_line(f"{n:4d}  {nodeid}")
+    terminalreporter.write_line(f"total {sum(n for _, n in _NEAR_TIES)} near-tie decisions in {len(_NEAR_TIES)} tests")
