@@ -668,7 +668,11 @@ __global__ void __launch_bounds__(kTcThreads) tree_attn_tc_kernel(
     constexpr uint32_t idesc_s = tc::idesc_bf16_f32(128, KB);
     constexpr uint32_t idesc_o = tc::idesc_bf16_f32_bmn(128, D);
     const uint32_t tS = taddr, tO = taddr + Lay::TMEM_O;
-    const uint32_t sq = smem_u32(smem);
+    // base descriptors stepped with desc_add: the integer work between MMAs is what
+    // bounds their issue rate from one thread
+    const uint64_t dq = tc::smem_desc_sw128(smem_u32(smem));
+    const uint64_t dkv0 = tc::smem_desc_sw128(smem_u32(smem + Lay::OFF_KV));
+    const uint64_t dv0 = tc::smem_desc_sw128_lbo_sbo(smem_u32(smem + Lay::OFF_KV + Lay::HALF), 8192, 1024);
     int ti = 0, si = 0;
     bool ok = true;
     int b = 0;
@@ -685,12 +689,11 @@ __global__ void __launch_bounds__(kTcThreads) tree_attn_tc_kernel(
           if (!tc::mbar_wait(p_full + (tix & 1), (tix >> 1) & 1)) { ok = false; return; }
           if (npv == 0 && si > 0 && !tc::mbar_wait(o_free, (si - 1) & 1)) { ok = false; return; }
           tc::fence_after_sync();
-          const uint32_t sp = smem_u32(smem + Lay::p_off(st, tix));
-          const uint32_t sv = smem_u32(smem + Lay::OFF_KV + st * Lay::STAGE + Lay::HALF);
+          const uint64_t dp = tc::smem_desc_sw128(smem_u32(smem + Lay::p_off(st, tix)));
+          const uint64_t dv = tc::desc_add(dv0, st * Lay::STAGE);
 #pragma unroll
           for (int kk = 0; kk < KB / 16; ++kk)
-            tc::mma_bf16(tO, tc::smem_desc_sw128(sp + kk * 32), tc::smem_desc_sw128_lbo_sbo(sv + kk * 2048, 8192, 1024),
-                         idesc_o, (npv | kk) != 0);
+            tc::mma_bf16(tO, tc::desc_add(dp, kk * 32), tc::desc_add(dv, kk * 2048), idesc_o, (npv | kk) != 0);
           tc::mma_commit(kv_empty + st);
           tc::mma_commit(pv_done);
           ++npv;
@@ -701,11 +704,11 @@ __global__ void __launch_bounds__(kTcThreads) tree_attn_tc_kernel(
           // S(ti) into buffer ti % 2: the softmax of tile ti-2 is done with it
           // (its P was waited for before PV(ti-2) was issued)
           tc::fence_after_sync();
-          const uint32_t sk = smem_u32(smem + Lay::OFF_KV + st * Lay::STAGE);
+          const uint64_t dk = tc::desc_add(dkv0, st * Lay::STAGE);
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk)
-            tc::mma_bf16(tS + (ti & 1) * KB, tc::smem_desc_sw128(sq + (kk >> 2) * 16384 + (kk & 3) * 32),
-                         tc::smem_desc_sw128(sk + (kk >> 2) * 8192 + (kk & 3) * 32), idesc_s, kk != 0);
+            tc::mma_bf16(tS + (ti & 1) * KB, tc::desc_add(dq, (kk >> 2) * 16384 + (kk & 3) * 32),
+                         tc::desc_add(dk, (kk >> 2) * 8192 + (kk & 3) * 32), idesc_s, kk != 0);
           tc::mma_commit(s_full + (ti & 1));
           if (k == nt - 1) tc::mma_commit(q_empty);
           if (k > 0) {

@@ -40,6 +40,12 @@ __device__ inline bool mbar_wait(uint64_t* bar, uint32_t parity) {
   }
 }
 
+// Ask for `bytes` (a multiple of 16, 16-byte aligned start) of global memory to
+// be brought into L2; a hint with no effect on the values any load returns.
+__device__ inline void prefetch_l2_bulk(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(p)), "r"(bytes) : "memory");
+}
+
 __device__ inline void prefetch_tmap(const CUtensorMap* m) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
 }
@@ -101,6 +107,13 @@ __device__ inline uint64_t smem_desc_sw128_lbo_sbo(uint32_t addr, uint32_t lbo, 
   return d;
 }
 
+// The descriptor of a tile `bytes` further on: the start address is the low 14
+// bits in 16-byte units, and shared-memory addresses stay below 2^18, so the
+// offset adds without carrying into the other fields.  Issuing MMAs from one
+// thread is bound by the integer work between them, so loops take one base
+// descriptor per stage and step it with this.
+__device__ __forceinline__ uint64_t desc_add(uint64_t d, uint32_t bytes) { return d + (bytes >> 4); }
+
 // Make this thread's generic-proxy shared-memory writes visible to the async
 // proxy (tensor core / TMA reads that follow a barrier).
 __device__ inline void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
@@ -122,6 +135,16 @@ __device__ inline void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
       "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
       " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n"
       ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate));
+}
+
+// The same with A from tensor memory: a_tmem is A's first column, row i of A in
+// lane i, bf16 pairs packed along K in each 32-bit column; B from shared memory.
+__device__ inline void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                   uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n"
+      ::"r"(d_tmem), "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate));
 }
 
 // Arrive on `bar` once every tcgen05 op issued so far by this thread has completed.
@@ -239,6 +262,15 @@ __device__ inline void tmem_st32(uint32_t taddr, const float (&v)[32]) {
         "r"(__float_as_uint(v[23])), "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])),
         "r"(__float_as_uint(v[26])), "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])),
         "r"(__float_as_uint(v[29])), "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
+      : "memory");
+}
+// Store 16 consecutive 32-bit columns of this thread's TMEM lane.
+__device__ inline void tmem_st16(uint32_t taddr, const uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"
+      ::"r"(taddr), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+        "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
       : "memory");
 }
 __device__ inline void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }

@@ -417,29 +417,33 @@ __global__ void __launch_bounds__(kTcThreads, 1) verify_tc_kernel(const __grid_c
   } else if (warp == kWarpMma) {
     if (lane == 0) {
       constexpr uint32_t idesc = tc::idesc_bf16_f32(BM, BN);
-      int i = 0, jl = 0;
+      // base descriptors of the rings, stepped with desc_add, and running stage
+      // and parity counters: the integer work between MMAs bounds their issue rate
+      const uint64_t da0 = tc::smem_desc_sw128(smem_u32(xsm)), db0 = tc::smem_desc_sw128(smem_u32(wsm));
+      int sw = 0, sx = 0;
+      uint32_t pw = 0, px = 0;
+      int jl = 0;
       bool run = true;
       for (int t = blockIdx.x; t < sh.n_tiles && run; t += gridDim.x, ++jl) {
         const int a = jl & 1;
         if (failed(&s_fail) || !tc::mbar_wait(acc_empty + a, ((jl >> 1) & 1) ^ 1)) { s_fail = 1; break; }
         tc::fence_after_sync();
         const uint32_t d = taddr + a * ACC_STRIDE;
-        for (int k = 0; k < nk; ++k, ++i) {
-          const int sw = i % sh.sw, sx = i % sh.sx;
-          if (failed(&s_fail) || !tc::mbar_wait(wfull + sw, (i / sh.sw) & 1) ||
-              !tc::mbar_wait(xfull + sx, (i / sh.sx) & 1)) {
+        for (int k = 0; k < nk; ++k) {
+          if (failed(&s_fail) || !tc::mbar_wait(wfull + sw, pw) || !tc::mbar_wait(xfull + sx, px)) {
             s_fail = 1;
             run = false;
             break;
           }
           tc::fence_after_sync();
-          const uint32_t sa = smem_u32(xsm + sx * kXStageBytes), sb = smem_u32(wsm + sw * W_BYTES);
+          const uint64_t da = tc::desc_add(da0, sx * kXStageBytes), db = tc::desc_add(db0, sw * W_BYTES);
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk)
-            tc::mma_bf16(d, tc::smem_desc_sw128(sa + kk * 32), tc::smem_desc_sw128(sb + kk * 32), idesc,
-                         (k | kk) != 0);
+            tc::mma_bf16(d, tc::desc_add(da, kk * 32), tc::desc_add(db, kk * 32), idesc, (k | kk) != 0);
           tc::mma_commit(wempty + sw);
           tc::mma_commit(xempty + sx);
+          if (++sw == sh.sw) { sw = 0; pw ^= 1; }
+          if (++sx == sh.sx) { sx = 0; px ^= 1; }
         }
         if (run) tc::mma_commit(acc_full + a);  // fires once every MMA of the tile has completed
       }

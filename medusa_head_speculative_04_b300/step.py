@@ -101,12 +101,14 @@ class MedusaStep:
     def capture(self, *args, prologue=None, epilogue=None, stream: Optional[torch.cuda.Stream] = None, **kwargs):
         """Capture one whole step (the arguments of :meth:`run`) in a CUDA graph.
 
-        The graph keeps the tensors it was captured with: refill them in place and
+        The graph reads the tensors it was captured with: refill them in place and
         ``replay()`` it to run the next step with one launch from the host.
         ``prologue`` and ``epilogue`` (callables, or None) are captured just before
-        and just after the step, on the same stream.  One eager step runs first, so
-        its outputs change state (``kv_len`` and the cache rows it commits) like any
-        other step.
+        and just after the step, on the same stream.  The returned graph holds
+        references to the arguments and to both callables (and so to the tensors
+        their closures use), so no buffer it reads can be freed and reused while it
+        lives.  One eager step runs first, so its outputs change state (``kv_len``
+        and the cache rows it commits) like any other step.
         """
         cur = torch.cuda.current_stream(self.device)
         s = stream if stream is not None else torch.cuda.Stream(self.device)  # capture needs a side stream
@@ -126,4 +128,5 @@ class MedusaStep:
             if epilogue is not None:
                 epilogue()
         cur.wait_stream(s)
+        g.medusa_keepalive = (args, kwargs, prologue, epilogue)
         return g

@@ -23,7 +23,7 @@ from _util import SMALL_BF16
 
 pytestmark = pytest.mark.gpu
 
-ACTIVATIONS = ("h", "X", "q", "k_new", "v_new", "root")
+ACTIVATIONS = ("h", "X", "q", "k_new", "v_new", "root")   # refilled before each replay
 
 
 @pytest.fixture(scope="module")
@@ -34,7 +34,11 @@ def mb():
 
 
 def timed_step(mb, wl, inp, temperature):
-    """The benchmark's step object and its captured graph (bench.py builds the same)."""
+    """The benchmark's step object and its captured graph (bench.py builds the same).
+
+    Every tensor the graph reads must outlive it, the source of the prologue's kv_len
+    reset included: it is returned with the rest (a freed source block could be handed
+    to the next allocation and the replay would copy whatever that holds)."""
     step = mb.MedusaStep(inp.choices, wl.B, wl.H, wl.V, wl.K, wl.Hq, wl.Hkv, wl.D, wl.Lmax, wl.k_needed(),
                          inp.dtype, kv_len_hint=max(wl.kv_lens()), keep_node_stats=False)
     assert step.head_logits is None and step.logits is None and step.node_p is None
@@ -45,6 +49,7 @@ def timed_step(mb, wl, inp, temperature):
     g = step.capture(act["h"], inp.W1, inp.b1, inp.W2, inp.lm_head, act["X"], act["q"], act["k_new"],
                      act["v_new"], kc, vc, kl, temperature, wl.posterior_threshold, wl.posterior_alpha,
                      root=act["root"], prologue=lambda: kl.copy_(kl0))
+    act["kv_len0"] = kl0
     return step, g, act, kc, vc, kl
 
 
