@@ -207,10 +207,29 @@ def tree_tokens(tt: TreeTables, root: np.ndarray, topk_ids: np.ndarray,
 # Tree attention  [WIB "Tree attention"; ULT "Tree attention and accepting tokens"]
 # ---------------------------------------------------------------------------
 
+def apply_rope(x: np.ndarray, positions: np.ndarray, theta: float) -> np.ndarray:
+    """Rotary position embedding, rotate-half form (Su et al., "RoFormer", 2021).
+
+    x [..., n, D] with positions [...] (one position per leading index, shared by
+    the n heads): for d < D/2, the pair (x[d], x[d + D/2]) is rotated by the angle
+    position * theta^(-2d/D).  Used to make the tree's position ids matter
+    [WIB "Tree attention": every candidate token gets its correct position index].
+    """
+    x = np.asarray(x, np.float64)
+    D = x.shape[-1]
+    half = D // 2
+    inv_freq = theta ** (-(2.0 * np.arange(half)) / D)
+    ang = np.asarray(positions, np.float64)[..., None, None] * inv_freq      # [..., 1, D/2]
+    c, s = np.cos(ang), np.sin(ang)
+    lo, hi = x[..., :half], x[..., half:]
+    return np.concatenate([lo * c - hi * s, hi * c + lo * s], axis=-1)
+
+
 def tree_attention(q: np.ndarray, k_new: np.ndarray, v_new: np.ndarray,
                    k_cache: np.ndarray, v_cache: np.ndarray, kv_len: np.ndarray,
                    tt: TreeTables, scale: float,
-                   only: Optional[Sequence[Tuple[int, int, int]]] = None) -> np.ndarray:
+                   only: Optional[Sequence[Tuple[int, int, int]]] = None,
+                   positions: Optional[np.ndarray] = None, rope_theta: float = 10000.0) -> np.ndarray:
     """One attention pass of all tree tokens over the KV cache plus the tree.
 
     Node i (query head hq) attends to the L = kv_len[b] cached keys and to
@@ -221,9 +240,14 @@ def tree_attention(q: np.ndarray, k_new: np.ndarray, v_new: np.ndarray,
 
     Reading: q/k/v are the layer's post-projection (post-RoPE) inputs, as the
     backbone that makes them is outside this step; query head hq uses key
-    head floor(hq * Hkv / Hq) (grouped-query attention).  ``only`` limits the
-    work to the listed (b, i, hq) outputs (others left NaN).
+    head floor(hq * Hkv / Hq) (grouped-query attention).  With ``positions``
+    [B, T] given, the tree's q and k_new are first rotated at those positions
+    (apply_rope); the cache keys are taken as already rotated at theirs.
+    ``only`` limits the work to the listed (b, i, hq) outputs (others left NaN).
     """
+    if positions is not None:
+        q = apply_rope(q, positions, rope_theta)
+        k_new = apply_rope(k_new, positions, rope_theta)
     B, T, Hq, D = q.shape
     Hkv = k_new.shape[2]
     out = np.full((B, T, Hq, D), np.nan)

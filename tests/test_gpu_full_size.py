@@ -53,3 +53,30 @@ def test_full_size_step(mb, name, variant, temperature, near_ties):
     assert near_ties(near) <= max(2, wl.B // 4)
     if variant == "plant":
         assert all(int(step.accept_len[b]) >= inp.plant["depths"][b] for b in range(wl.B))
+
+
+# Tree-size sweep at the Vicuna-7B shape: the bench's 64-node tree is covered by the
+# 7B parity tests; these are the larger trees of the sweep (a seeded 256-node sparse
+# tree and the full 10 x 10 x 10 product tree, T = 1111), where the verification
+# GEMM has several row tiles and attention several query tiles per head.
+TREES = [("seeded256", ("seeded", 256, (10, 6, 4, 2, 1)), "plant", 0.7),
+         ("cartesian10x10x10", ("cartesian", (10, 10, 10)), "random", 0.0),
+         ("cartesian10x10x10", ("cartesian", (10, 10, 10)), "plant", 0.7)]
+
+
+@pytest.mark.parametrize("tree_name,tree,variant,temperature", TREES, ids=lambda v: str(v) if not isinstance(v, tuple) else None)
+def test_vicuna7b_tree_sizes(mb, tree_name, tree, variant, temperature, near_ties):
+    import dataclasses
+    wl = dataclasses.replace(synth.WORKLOADS["vicuna7b"], name=f"vicuna7b_{tree_name}", tree=tree)
+    inp, step, kc, vc, kl = run(mb, wl, variant, temperature)
+    tt = oracle.tree_tables(inp.choices)
+    assert tt.T == {"seeded256": 257, "cartesian10x10x10": 1111}[tree_name]
+    near = check_heads(wl, inp, step)
+    check_tree(wl, inp, step, tt)
+    check_attention(wl, inp, step, tt)
+    near += check_verify_accept(wl, inp, step, tt, temperature, sample_rows=8)
+    check_commit(wl, inp, step, kc, vc, kl, tt)
+    assert int((step.dev_status & ~1).max()) == 0
+    assert near_ties(near) <= 2
+    if variant == "plant":
+        assert int(step.accept_len[0]) >= inp.plant["depths"][0]

@@ -205,6 +205,71 @@ def test_tree_attention_zero_query_is_mean():
         np.testing.assert_allclose(o[0, i, 0], np.mean(vis, axis=0), atol=1e-14)
 
 
+# --------------------------------------------------------------------------- rotary positions
+
+def test_rope_hand_values():
+    """Rotate-half rotary embedding (RoFormer): D = 2, x = (1, 0) at position 1 turns by
+    1 radian -> (cos 1, sin 1); D = 4, theta = 10000 at position 2: the pair (x0, x2)
+    turns by 2 rad and (x1, x3) by 2 * 10000^(-1/2) = 0.02 rad.  Values written out by hand."""
+    got = oracle.apply_rope(np.array([[[1.0, 0.0]]]), np.array([1]), 10000.0)[0, 0]
+    np.testing.assert_allclose(got, [0.5403023058681398, 0.8414709848078965], rtol=0, atol=1e-15)
+    got = oracle.apply_rope(np.array([[[1.0, 2.0, 3.0, 4.0]]]), np.array([2]), 10000.0)[0, 0]
+    want = [-3.1440391170241875, 1.9196053465598233, -0.33914308281574557, 4.039197360052977]
+    np.testing.assert_allclose(got, want, rtol=0, atol=1e-14)
+
+
+def test_rope_is_complex_rotation():
+    """The same map as multiplying z_d = x_d + i x_(d+D/2) by exp(i p theta^(-2d/D))
+    (an independent formulation: a swapped sign or half would fail it)."""
+    r = _rng(11)
+    x = r.standard_normal((3, 5, 2, 8))
+    pos = r.integers(0, 5000, size=(3, 5))
+    got = oracle.apply_rope(x, pos, 500.0)
+    z = x[..., :4] + 1j * x[..., 4:]
+    w = z * np.exp(1j * pos[..., None, None] * 500.0 ** (-(2.0 * np.arange(4)) / 8))
+    np.testing.assert_allclose(got, np.concatenate([w.real, w.imag], axis=-1), rtol=0, atol=1e-12)
+
+
+def test_rope_scores_depend_on_relative_position_only():
+    """q(m) . k(n) after rotation depends on m - n alone (q and k turned the same way),
+    position 0 leaves a vector unchanged, and every rotation keeps the norm."""
+    r = _rng(12)
+    q, k = r.standard_normal((1, 1, 1, 16)), r.standard_normal((1, 1, 1, 16))
+    s = lambda m, n: float(np.sum(oracle.apply_rope(q, np.array([[m]]), 10000.0) *
+                                  oracle.apply_rope(k, np.array([[n]]), 10000.0)))
+    assert abs(s(7, 3) - s(1007, 1003)) < 1e-10 and abs(s(7, 3) - s(3, 7)) > 1e-3
+    np.testing.assert_array_equal(oracle.apply_rope(q, np.array([[0]]), 10000.0), q)
+    assert abs(np.linalg.norm(oracle.apply_rope(q, np.array([[123]]), 10000.0)) - np.linalg.norm(q)) < 1e-12
+
+
+def test_tree_attention_with_positions_equals_rotated_paths():
+    """With position ids, every root->leaf path run as a causal sequence after the cache, its
+    query and key rows first turned by the complex rotation at positions L + depth, gives each
+    node the output of the tree-masked pass."""
+    r = _rng(13)
+    tt = oracle.tree_tables(synth.cartesian_choices((2, 3)))
+    B, T, Hq, Hkv, D, Lmax = 1, tt.T, 2, 1, 8, 9
+    q, kn, vn = r.standard_normal((B, T, Hq, D)), r.standard_normal((B, T, Hkv, D)), r.standard_normal((B, T, Hkv, D))
+    kc, vc = r.standard_normal((B, Hkv, Lmax, D)), r.standard_normal((B, Hkv, Lmax, D))
+    L = 5
+    pos = np.array([[L + len(n) for n in tt.nodes]])
+    o = oracle.tree_attention(q, kn, vn, kc, vc, np.array([L]), tt, 0.5, positions=pos, rope_theta=100.0)
+
+    def turn(v, p):
+        z = v[:4] + 1j * v[4:]
+        w = z * np.exp(1j * p * 100.0 ** (-(2.0 * np.arange(4)) / D))
+        return np.concatenate([w.real, w.imag])
+
+    qr = np.array([[turn(q[0, i, h], pos[0, i]) for h in range(Hq)] for i in range(T)])[None]
+    kr = np.array([[turn(kn[0, i, 0], pos[0, i])] for i in range(T)])[None]
+    for leaf in tt.leaves:
+        path = tt.ancestors[leaf] + [leaf]
+        for hq in range(Hq):
+            brute = _path_attention_brute(qr[0], kr[0], vn[0], kc[0], vc[0], L, path, hq, Hq // Hkv, 0.5)
+            for node, ob in zip(path, brute):
+                np.testing.assert_allclose(o[0, node, hq], ob, rtol=0, atol=1e-12)
+
+
 def test_verify_logits_hand_values():
     """lm_head [V, H] rows dotted with each tree node's state: rows (1,2),(3,4),(5,6) give
     (1,3,5) for x = (1,0) and (-1,-1,-1) for x = (1,-1)."""
