@@ -111,6 +111,12 @@ typedef struct {
 int medusa_tree_create(const int32_t* ranks_flat_host, const int32_t* lens_host,
                        int32_t n_choices, medusa_tree** out);
 int medusa_tree_get_info(const medusa_tree* tree, medusa_tree_info* info);
+/* The tree's sizes one by one (any pointer may be NULL): T nodes including the
+ * root, P paths, dmax, and topk_per_depth[MEDUSA_MAX_DEPTH]: entry d is the
+ * number of top-k candidates head d+1 must supply (largest rank used at depth
+ * d+1, plus one; 0 past dmax). */
+int medusa_tree_query(const medusa_tree* tree, int32_t* T, int32_t* P, int32_t* dmax,
+                      int32_t* topk_per_depth);
 /* Host copies of the tables (any pointer may be NULL): parent[T] (-1 root),
  * depth[T], rank[T] (-1 root), mask[T * mask_words] (bit j of row i set iff
  * node j is i or an ancestor of i), paths[P * (dmax+1)] (node ids root->leaf,
@@ -206,25 +212,39 @@ int medusa_build_tree(const medusa_tree* tree, const int32_t* root_tok, const in
  * One attention pass of all tree tokens over the KV cache plus the tree:
  * node i attends to the kv_len[b] cached keys and to the tree keys of its
  * ancestors and itself only (wiblog "Tree attention": each token may attend
- * only to the tokens on its own prefix path; Ultralytics "Tree attention
- * and accepting tokens").  o = softmax(scale * q k^T) v.
+ * only to the tokens on its own prefix path, every token with its correct
+ * position index; Ultralytics "Tree attention and accepting tokens").
+ * o = softmax(scale * q k^T) v.
  *   q [B,T,Hq,D]; k_new, v_new [B,T,Hkv,D]; k_cache, v_cache [B,Hkv,Lmax,D];
  *   kv_len [B] device, each in [0, Lmax]; out [B,T,Hq,D] fp32.
  *   Query head hq reads key/value head hq / (Hq/Hkv) (grouped-query attention).
- *   q/k/v are taken as given (position encoding, if any, already applied).
+ *   Position encoding (no counterpart on the pages beyond "correct position
+ *   index"; rotary embedding as in Su et al., "RoFormer", 2021):
+ *     rope == 0: q and k_new are taken as given, already position-encoded
+ *       (the layer that produces them is outside this library);
+ *       position_ids is unused and may be NULL.
+ *     rope != 0: q and k_new are first rotated at position_ids [B,T] int32
+ *       (device; medusa_build_tree's output, kv_len + depth), rotate-half
+ *       form: for d < D/2 the pair (x[d], x[d+D/2]) turns by
+ *       position * rope_theta^(-2d/D) (rope_theta > 1, e.g. 10000).  The cache
+ *       keys are taken as already rotated at their own positions.  When k_rot
+ *       is not NULL the rotated keys [B,T,Hkv,D] (dtype) are written there, so
+ *       that medusa_kv_commit can append rotated keys to the cache; otherwise
+ *       they stay in the workspace.
  *   kv_len_hint: host upper bound of kv_len (0 = Lmax); used only to size the
  *   split of the cache across CTAs, any kv_len <= Lmax is handled.
  *   Limits: D in {64, 128}; Hq % Hkv == 0; Hq <= 128.
+ *   After MEDUSA_DEV_TIMEOUT the workspace must be zero-filled again.
  * ---------------------------------------------------------------------- */
 size_t medusa_tree_attention_workspace_size(const medusa_tree* tree, int32_t B, int32_t Hq,
                                             int32_t Hkv, int32_t D, int32_t Lmax,
                                             int32_t kv_len_hint, medusa_dtype dtype);
 int medusa_tree_attention(const medusa_tree* tree, const void* q, const void* k_new,
                           const void* v_new, const void* k_cache, const void* v_cache,
-                          const int32_t* kv_len, int32_t B, int32_t Hq, int32_t Hkv, int32_t D,
-                          int32_t Lmax, int32_t kv_len_hint, float scale, medusa_dtype dtype,
-                          float* out, void* ws, size_t ws_bytes, int32_t* dev_status,
-                          medusa_stream_t stream);
+                          const int32_t* kv_len, const int32_t* position_ids, int32_t B, int32_t Hq,
+                          int32_t Hkv, int32_t D, int32_t Lmax, int32_t kv_len_hint, float scale,
+                          int32_t rope, float rope_theta, medusa_dtype dtype, float* out, void* k_rot,
+                          void* ws, size_t ws_bytes, int32_t* dev_status, medusa_stream_t stream);
 
 /* ------------------------------------------------------------------------
  * medusa_verify_accept

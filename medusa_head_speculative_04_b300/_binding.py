@@ -71,8 +71,9 @@ _sig("medusa_heads_topk_noalloc", ctypes.c_int,
 _sig("medusa_build_tree", ctypes.c_int, [_vp, _vp, _vp, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _vp])
 _sig("medusa_tree_attention_workspace_size", _sz, [_vp, _i32, _i32, _i32, _i32, _i32, _i32, ctypes.c_int])
 _sig("medusa_tree_attention", ctypes.c_int,
-     [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _f32, ctypes.c_int, _vp, _vp, _sz,
-      _vp, _vp])
+     [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _f32, _i32, _f32, ctypes.c_int, _vp,
+      _vp, _vp, _sz, _vp, _vp])
+_sig("medusa_tree_query", ctypes.c_int, [_vp, _vp, _vp, _vp, _vp])
 _sig("medusa_verify_accept_workspace_size", _sz, [_vp, _i32, _i32, _i32, ctypes.c_int])
 _sig("medusa_verify_accept", ctypes.c_int,
      [_vp, _vp, _vp, _vp, _i32, _i32, _i32, ctypes.c_int, _f32, _f32, _f32, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
@@ -127,6 +128,13 @@ class Tree:
     @property
     def handle(self):
         return self._h
+
+    def query(self):
+        """(T, P, dmax, top-k each head must supply) from medusa_tree_query."""
+        T, P, dm = _i32(), _i32(), _i32()
+        tk = (_i32 * MAX_DEPTH)()
+        _check("medusa_tree_query", lib.medusa_tree_query(self._h, ctypes.byref(T), ctypes.byref(P), ctypes.byref(dm), tk))
+        return T.value, P.value, dm.value, list(tk)[: dm.value]
 
     def tables(self):
         T, P, W, MW = self.T, self.P, self.dmax + 1, self.mask_words
@@ -198,14 +206,15 @@ def medusa_tree_attention_workspace_size(tree: Tree, B, Hq, Hkv, D, Lmax, kv_len
 
 
 def medusa_tree_attention(tree: Tree, q, k_new, v_new, k_cache, v_cache, kv_len, out, ws, scale: float,
-                          kv_len_hint: int = 0, dev_status=None, stream=None) -> None:
+                          kv_len_hint: int = 0, dev_status=None, stream=None, position_ids=None, rope: bool = False,
+                          rope_theta: float = 10000.0, k_rot=None) -> None:
     B, T, Hq, D = q.shape
     Hkv = k_new.shape[2]
     Lmax = k_cache.shape[2]
     _check("medusa_tree_attention", lib.medusa_tree_attention(
-        tree.handle, _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache), _ptr(kv_len), B, Hq, Hkv,
-        D, Lmax, kv_len_hint, scale, dtype_code(q), _ptr(out), _ptr(ws), ws.numel() if ws is not None else 0,
-        _ptr(dev_status), _stream(stream)))
+        tree.handle, _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache), _ptr(kv_len),
+        _ptr(position_ids), B, Hq, Hkv, D, Lmax, kv_len_hint, scale, int(bool(rope)), rope_theta, dtype_code(q),
+        _ptr(out), _ptr(k_rot), _ptr(ws), ws.numel() if ws is not None else 0, _ptr(dev_status), _stream(stream)))
 
 
 def medusa_verify_accept_workspace_size(tree: Tree, B, H, V, dtype_c) -> int:

@@ -26,6 +26,7 @@
 // partial's loads in flight at once).
 // fp32 path: an exact scalar kernel (small shapes).
 #include <algorithm>
+#include <cmath>
 
 #include "tc.cuh"
 #include "tree.cuh"
@@ -1005,6 +1006,39 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(AttnArgs a, int attn_
   if (lane == 0 && !(den > 0.f) && a.dev_status) atomicOr(a.dev_status + b, MEDUSA_DEV_NAN);
 }
 
+// Rotary position embedding of the tree's queries and keys (rotate-half form,
+// Su et al., "RoFormer", 2021): for d < D/2 the pair (x[d], x[d + D/2]) turns by
+// position * theta^(-2d/D).  One CTA per tree node; the D/2 angles are computed
+// once per node in double precision (positions reach the tens of thousands) and
+// shared by every head of the node.
+template <typename T>
+__global__ void __launch_bounds__(256) rope_kernel(const T* __restrict__ q, const T* __restrict__ k,
+                                                   const int32_t* __restrict__ pos, int Hq, int Hkv, int D,
+                                                   double log2_theta, T* __restrict__ q_out, T* __restrict__ k_out) {
+  __shared__ float s_c[64], s_s[64];
+  const size_t node = blockIdx.x;  // b * T + i
+  const int half = D / 2;
+  pdl_wait();
+  pdl_trigger();
+  if (static_cast<int>(threadIdx.x) < half) {
+    const double ang = static_cast<double>(pos[node]) * exp2(-(2.0 * threadIdx.x / D) * log2_theta);
+    double sn, cs;
+    sincos(ang, &sn, &cs);
+    s_c[threadIdx.x] = static_cast<float>(cs);
+    s_s[threadIdx.x] = static_cast<float>(sn);
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < (Hq + Hkv) * half; e += blockDim.x) {
+    const int h = e / half, d = e % half;
+    const T* src = h < Hq ? q + (node * Hq + h) * D : k + (node * Hkv + (h - Hq)) * D;
+    T* dst = h < Hq ? q_out + (node * Hq + h) * D : k_out + (node * Hkv + (h - Hq)) * D;
+    const float x0 = Elem<T>::to_f(src[d]), x1 = Elem<T>::to_f(src[d + half]);
+    const float c = s_c[d], sn = s_s[d];
+    dst[d] = Elem<T>::from_f(fmaf(x0, c, -x1 * sn));
+    dst[d + half] = Elem<T>::from_f(fmaf(x1, c, x0 * sn));
+  }
+}
+
 // Exact fp32 path: one CTA per (request, node, query head); scores in smem.
 __global__ void __launch_bounds__(128) tree_attn_f32_kernel(medusa_tree_dev tr, const float* __restrict__ q,
                                                             const float* __restrict__ k_new,
@@ -1072,13 +1106,20 @@ __global__ void __launch_bounds__(128) tree_attn_f32_kernel(medusa_tree_dev tr, 
 
 }  // namespace
 
+// Bytes of the rotated queries and keys held ahead of the split partials in the workspace.
+size_t rope_ws_bytes(int B, int T, int Hq, int Hkv, int D, int es) {
+  return align_up(static_cast<size_t>(B) * T * Hq * D * es, 256) + align_up(static_cast<size_t>(B) * T * Hkv * D * es, 256);
+}
+
 MEDUSA_API size_t medusa_tree_attention_workspace_size(const medusa_tree* tree, int32_t B, int32_t Hq, int32_t Hkv,
                                                        int32_t D, int32_t Lmax, int32_t kv_len_hint,
                                                        medusa_dtype dtype) {
   if (!tree || B < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv || Lmax < 0) return 0;
-  if (dtype == MEDUSA_F32) return 256;
+  if (D != 64 && D != 128) return 0;
+  const size_t rope = rope_ws_bytes(B, tree->T, Hq, Hkv, D, dtype == MEDUSA_BF16 ? 2 : 4);
+  if (dtype == MEDUSA_F32) return rope;
   AttnPlan p = plan_attn(tree->T, B, Hq, Hkv, Lmax, kv_len_hint, device_sm_count());
-  return carve_attn_ws(nullptr, p, D).bytes;
+  return rope + carve_attn_ws(nullptr, p, D).bytes;
 }
 
 namespace {
@@ -1155,20 +1196,51 @@ int launch_attn_bf16(const medusa_tree* tree, const void* q, const void* k_new, 
 }  // namespace
 
 MEDUSA_API int medusa_tree_attention(const medusa_tree* tree, const void* q, const void* k_new, const void* v_new,
-                                     const void* k_cache, const void* v_cache, const int32_t* kv_len, int32_t B,
-                                     int32_t Hq, int32_t Hkv, int32_t D, int32_t Lmax, int32_t kv_len_hint,
-                                     float scale, medusa_dtype dtype, float* out, void* ws, size_t ws_bytes,
+                                     const void* k_cache, const void* v_cache, const int32_t* kv_len,
+                                     const int32_t* position_ids, int32_t B, int32_t Hq, int32_t Hkv, int32_t D,
+                                     int32_t Lmax, int32_t kv_len_hint, float scale, int32_t rope, float rope_theta,
+                                     medusa_dtype dtype, float* out, void* k_rot, void* ws, size_t ws_bytes,
                                      int32_t* dev_status, medusa_stream_t stream) {
   if (!tree || !q || !k_new || !v_new || !k_cache || !v_cache || !kv_len || !out) return MEDUSA_ERR_INVALID_ARG;
   if (B < 1 || B > MEDUSA_MAX_BATCH || Hq < 1 || Hkv < 1 || Lmax < 0 || Hq > 128) return MEDUSA_ERR_INVALID_ARG;
   if (dtype != MEDUSA_F32 && dtype != MEDUSA_BF16) return MEDUSA_ERR_INVALID_ARG;
+  if (rope && (!position_ids || !(rope_theta > 1.f))) return MEDUSA_ERR_INVALID_ARG;
   if (Hq % Hkv != 0 || (D != 64 && D != 128)) return MEDUSA_ERR_UNSUPPORTED;
   const void* ptrs[] = {q, k_new, v_new, k_cache, v_cache, kv_len, out};
   for (const void* x : ptrs)
     if (!aligned16(x)) return MEDUSA_ERR_ALIGNMENT;
-  if ((ws && !aligned16(ws)) || (dev_status && !aligned16(dev_status))) return MEDUSA_ERR_ALIGNMENT;
+  const void* opt[] = {ws, dev_status, position_ids, k_rot};
+  for (const void* x : opt)
+    if (x && !aligned16(x)) return MEDUSA_ERR_ALIGNMENT;
   auto st = reinterpret_cast<cudaStream_t>(stream);
   const int T = tree->T;
+  const int es = dtype == MEDUSA_BF16 ? 2 : 4;
+  const size_t rope_bytes = rope_ws_bytes(B, T, Hq, Hkv, D, es);
+  char* wsc = static_cast<char*>(ws);
+  if (rope) {
+    // q and k_new rotated at the tree's position ids into the workspace (k into
+    // k_rot when the caller keeps the rotated keys, e.g. to commit them)
+    if (!ws || ws_bytes < rope_bytes) return MEDUSA_ERR_WORKSPACE;
+    void* q_r = wsc;
+    void* k_r = k_rot ? k_rot : wsc + align_up(static_cast<size_t>(B) * T * Hq * D * es, 256);
+    const double l2t = std::log2(static_cast<double>(rope_theta));
+    cudaError_t e;
+    if (dtype == MEDUSA_BF16)
+      e = launch_pdl(rope_kernel<__nv_bfloat16>, dim3(B * T), dim3(256), 0, st, static_cast<const __nv_bfloat16*>(q),
+                     static_cast<const __nv_bfloat16*>(k_new), position_ids, Hq, Hkv, D, l2t,
+                     static_cast<__nv_bfloat16*>(q_r), static_cast<__nv_bfloat16*>(k_r));
+    else
+      e = launch_pdl(rope_kernel<float>, dim3(B * T), dim3(256), 0, st, static_cast<const float*>(q),
+                     static_cast<const float*>(k_new), position_ids, Hq, Hkv, D, l2t, static_cast<float*>(q_r),
+                     static_cast<float*>(k_r));
+    if (e != cudaSuccess) {
+      (void)cudaGetLastError();
+      return MEDUSA_ERR_CUDA;
+    }
+    MEDUSA_LAUNCH_CHECK();
+    q = q_r;
+    k_new = k_r;
+  }
   if (dtype == MEDUSA_F32) {
     const size_t smem = static_cast<size_t>(Lmax + T) * 4;
     if (smem > 200 * 1024) return MEDUSA_ERR_UNSUPPORTED;
@@ -1185,8 +1257,8 @@ MEDUSA_API int medusa_tree_attention(const medusa_tree* tree, const void* q, con
     return MEDUSA_OK;
   }
   AttnPlan p = plan_attn(T, B, Hq, Hkv, Lmax, kv_len_hint, device_sm_count());
-  AttnWs w = carve_attn_ws(ws, p, D);
-  if (!ws || ws_bytes < w.bytes) return MEDUSA_ERR_WORKSPACE;
+  AttnWs w = carve_attn_ws(wsc ? wsc + rope_bytes : nullptr, p, D);
+  if (!ws || ws_bytes < rope_bytes + w.bytes) return MEDUSA_ERR_WORKSPACE;
   if (D == 128)
     return launch_attn_bf16<128>(tree, q, k_new, v_new, k_cache, v_cache, kv_len, B, Hq, Hkv, Lmax, scale, out, p, w,
                                  dev_status, st);

@@ -166,6 +166,16 @@ MEDUSA_API int medusa_tree_get_info(const medusa_tree* t, medusa_tree_info* info
   return MEDUSA_OK;
 }
 
+MEDUSA_API int medusa_tree_query(const medusa_tree* t, int32_t* T, int32_t* P, int32_t* dmax, int32_t* topk_per_depth) {
+  if (!t) return MEDUSA_ERR_INVALID_ARG;
+  if (T) *T = t->T;
+  if (P) *P = t->P;
+  if (dmax) *dmax = t->dmax;
+  if (topk_per_depth)
+    for (int d = 0; d < MEDUSA_MAX_DEPTH; ++d) topk_per_depth[d] = d < t->dmax ? t->max_rank[d] + 1 : 0;
+  return MEDUSA_OK;
+}
+
 MEDUSA_API int medusa_tree_copy_tables(const medusa_tree* t, int32_t* parent, int32_t* depth, int32_t* rank,
                                        uint32_t* mask, int32_t* paths) {
   if (!t) return MEDUSA_ERR_INVALID_ARG;

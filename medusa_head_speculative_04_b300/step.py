@@ -20,13 +20,17 @@ from . import _binding as mb
 class MedusaStep:
     def __init__(self, choices: Sequence[Sequence[int]], B: int, H: int, V: int, K: int, Hq: int, Hkv: int,
                  D: int, Lmax: int, topk: int, dtype: torch.dtype, device="cuda", root_from_lm_head=False,
-                 kv_len_hint: int = 0, keep_head_logits=False, keep_logits=False, keep_node_stats=True):
+                 kv_len_hint: int = 0, keep_head_logits=False, keep_logits=False, keep_node_stats=True,
+                 rope: bool = False, rope_theta: float = 10000.0):
         self.tree = mb.Tree(choices)
         self.B, self.H, self.V, self.K = B, H, V, K
         self.Hq, self.Hkv, self.D, self.Lmax, self.topk = Hq, Hkv, D, Lmax, topk
         self.dtype, self.device = dtype, torch.device(device)
         self.root_from_lm_head = root_from_lm_head
         self.kv_len_hint = kv_len_hint
+        # rope: the tree's q and k are rotated at the position ids the tree expansion
+        # produced, and the rotated keys are what the commit appends to the cache
+        self.rope, self.rope_theta = rope, rope_theta
         T, P, W = self.tree.T, self.tree.P, self.tree.dmax + 1
         dc = mb.MEDUSA_BF16 if dtype == torch.bfloat16 else mb.MEDUSA_F32
         i32 = dict(dtype=torch.int32, device=self.device)
@@ -38,6 +42,7 @@ class MedusaStep:
         self.positions = torch.zeros(B, T, **i32)
         self.candidates = torch.zeros(B, P, W, **i32)
         self.attn_out = torch.zeros(B, T, Hq, D, **f32)
+        self.k_rot = torch.zeros(B, T, Hkv, D, dtype=dtype, device=self.device) if rope else None
         # the per-request results share one buffer, so a caller can read them with one copy;
         # each part starts on a 16-byte boundary, as the C entry points require
         Bp = (B + 3) // 4 * 4
@@ -74,7 +79,8 @@ class MedusaStep:
     def attention(self, q, k_new, v_new, k_cache, v_cache, kv_len, stream=None):
         mb.medusa_tree_attention(self.tree, q, k_new, v_new, k_cache, v_cache, kv_len, self.attn_out,
                                  self.ws_attn, 1.0 / math.sqrt(self.D), kv_len_hint=self.kv_len_hint,
-                                 dev_status=self.dev_status, stream=stream)
+                                 dev_status=self.dev_status, stream=stream, position_ids=self.positions,
+                                 rope=self.rope, rope_theta=self.rope_theta, k_rot=self.k_rot)
 
     def verify(self, X, lm_head, temperature: float, threshold: float = 0.09, alpha: float = 0.3, stream=None):
         mb.medusa_verify_accept(self.tree, X, lm_head, self.tokens, temperature, threshold, alpha,
@@ -83,7 +89,8 @@ class MedusaStep:
                                 node_H=self.node_H, dev_status=self.dev_status, stream=stream)
 
     def commit(self, k_new, v_new, k_cache, v_cache, kv_len, stream=None):
-        mb.medusa_kv_commit(self.tree, k_new, v_new, k_cache, v_cache, kv_len, self.best_node,
+        mb.medusa_kv_commit(self.tree, self.k_rot if self.rope else k_new, v_new, k_cache, v_cache, kv_len,
+                            self.best_node,
                             dev_status=self.dev_status, stream=stream)
 
     def run(self, h, W1, b1, W2, lm_head, X, q, k_new, v_new, k_cache, v_cache, kv_len, temperature: float,

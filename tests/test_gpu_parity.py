@@ -291,3 +291,50 @@ def test_missing_candidate_flags_bad_token(mb):
     tok_o, pos_o = oracle.tree_tokens(tt, npi(inp.root), npi(ids), npi(inp.kv_len))
     assert np.array_equal(npi(tokens), tok_o)       # the -1 is passed through, not replaced
     assert np.array_equal(npi(pos), pos_o)
+
+
+# ----------------------------------------------------------------------------- positions
+
+def test_tree_query_sizes(mb):
+    """medusa_tree_query on the 2 x 3 product tree: 9 nodes, 6 paths, depth 2, and heads 1
+    and 2 must supply their top-2 and top-3 (wiblog "Tree attention" worked example)."""
+    tree = mb.Tree(synth.cartesian_choices((2, 3)))
+    assert tree.query() == (9, 6, 2, [2, 3])
+
+
+@pytest.mark.parametrize("name", ["tiny", "small_bf16"])
+def test_rope_step_matches_oracle(mb, name, near_ties):
+    """With rotary position encoding, the tree's q and k are turned at the position ids the
+    tree expansion produced: attention outputs match the oracle's rotated pass, the rotated
+    keys match apply_rope, the committed cache rows are the rotated keys, and the outputs
+    differ from the unrotated pass (positions matter)."""
+    wl = synth.WORKLOADS["tiny"] if name == "tiny" else SMALL_BF16
+    kind = wl.dtype
+    inp = synth.make_inputs(wl, "cuda", variant="plant", plant_depth=2 if name == "tiny" else None)
+    step = make_step(mb, wl, inp, rope=True, rope_theta=10000.0)
+    kc, vc, kl = inp.k_cache.clone(), inp.v_cache.clone(), inp.kv_len.clone()
+    step.run(inp.h, inp.W1, inp.b1, inp.W2, inp.lm_head, inp.X, inp.q, inp.k_new, inp.v_new, kc, vc, kl,
+             0.7, wl.posterior_threshold, wl.posterior_alpha, root=inp.root)
+    torch.cuda.synchronize()
+    o = step_oracle_inputs(inp)
+    tt = oracle.tree_tables(inp.choices)
+    pos = npi(step.positions)
+    _, pos_o = oracle.tree_tokens(tt, npi(step.root), npi(step.topk_ids), npi(inp.kv_len))
+    assert np.array_equal(pos, pos_o)
+    a_o = oracle.tree_attention(o["q"], o["k_new"], o["v_new"], o["k_cache"], o["v_cache"], npi(inp.kv_len), tt,
+                                1.0 / math.sqrt(wl.D), positions=pos_o, rope_theta=10000.0)
+    assert rel_err(step.attn_out, a_o) < TOL[kind]
+    a_plain = oracle.tree_attention(o["q"], o["k_new"], o["v_new"], o["k_cache"], o["v_cache"], npi(inp.kv_len), tt,
+                                    1.0 / math.sqrt(wl.D))
+    assert rel_err(step.attn_out, a_plain) > 10 * TOL[kind]
+    k_o = oracle.apply_rope(o["k_new"], pos_o, 10000.0)
+    assert rel_err(step.k_rot, k_o) < (1e-5 if kind == "f32" else 1e-2)
+    # the commit appended the rotated keys (bit-exact copies of k_rot) and the plain values
+    kl0 = npi(inp.kv_len)
+    for b in range(wl.B):
+        best = int(step.best_node[b])
+        chain = tt.ancestors[best] + [best]
+        for d, node in enumerate(chain):
+            assert torch.equal(kc[b, :, kl0[b] + d], step.k_rot[b, node])
+            assert torch.equal(vc[b, :, kl0[b] + d], inp.v_new[b, node])
+    near_ties(0)
