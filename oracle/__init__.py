@@ -28,7 +28,7 @@ a fact the pages or mathematics fix (see tests/test_oracle_pins.py), except
 where a function's docstring says "parity unpinned".
 """
 from .medusa import (  # noqa: F401
-    bf16_round, medusa_heads, head_topk, base_root,
+    bf16_round, medusa_heads, tree_heads, head_topk, base_root,
     TreeTables, tree_tables, tree_tokens,
     apply_rope, tree_attention, verify_logits, node_posterior, typical_accept, kv_commit,
     run_step, StepResult,

@@ -68,6 +68,20 @@ def medusa_heads(h: np.ndarray, W1: np.ndarray, b1: np.ndarray, W2: np.ndarray,
     return u, z
 
 
+def tree_heads(X: np.ndarray, best_node: np.ndarray, W1: np.ndarray, b1: np.ndarray, W2: np.ndarray,
+               u_bf16: bool) -> Tuple[np.ndarray, np.ndarray]:
+    """The heads on the accepted node's hidden state, which the next step's
+    candidates come from [WIB "Inference flow in an online chat service": the
+    verification pass yields the next round's candidates with no extra pass;
+    ULT "Tree attention and accepting tokens": the accepted branch continues].
+    X [B, T, H] holds every tree node's state; row best_node[b] of request b
+    goes through medusa_heads.  Returns (u, logits) as medusa_heads does.
+    """
+    X = np.asarray(X, np.float64)
+    rows = X[np.arange(X.shape[0]), np.asarray(best_node)]
+    return medusa_heads(rows, W1, b1, W2, u_bf16)
+
+
 def head_topk(z: np.ndarray, k: int) -> Tuple[np.ndarray, np.ndarray, np.ndarray]:
     """Top-k candidates of each head's logits [WIB "Medusa decoding heads"; JIS].
 

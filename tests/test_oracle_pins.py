@@ -61,6 +61,37 @@ def test_silu_negative_branch():
     assert abs(u[0, 0, 0] - (-0.2689414213699951)) < 1e-15
 
 
+def test_tree_heads_zero_init_is_the_accepted_rows_verification():
+    """Heads over the tree nodes keep the accepted node's row: with the heads' start state
+    (W1 = b1 = 0, W2_k = lm_head; Ultralytics "Medusa Heads" example) every head's logits on
+    that row equal the verification logits of the accepted node exactly."""
+    r = _rng(21)
+    B, T, H, V, K = 2, 5, 6, 11, 3
+    X = r.standard_normal((B, T, H))
+    lm = r.standard_normal((V, H)) * 0.02
+    best = np.array([3, 0])
+    _, z = oracle.tree_heads(X, best, np.zeros((K, H, H)), np.zeros((K, H)), np.broadcast_to(lm, (K, V, H)), False)
+    zv = oracle.verify_logits(X, lm)
+    for b in range(B):
+        for k in range(K):
+            assert np.array_equal(z[b, k], zv[b, best[b]])
+
+
+def test_tree_heads_reads_only_the_accepted_row():
+    """The other tree rows do not enter (changing them leaves the result), and the accepted
+    row gives the hand values of the head formula (x = (1, 1) -> u = (1 + SiLU(3.5), 1))."""
+    W1 = np.array([[[1.0, 2.0], [0.0, 1.0]]])
+    b1 = np.array([[0.5, -1.0]])
+    W2 = np.array([[[1.0, 0.0], [0.0, 1.0], [1.0, -1.0]]])
+    X = np.array([[[7.0, -3.0], [1.0, 1.0], [0.0, 2.0]]])
+    u, z = oracle.tree_heads(X, np.array([1]), W1, b1, W2, False)
+    silu35 = 3.3974071923702527
+    np.testing.assert_allclose(z[0, 0], [1.0 + silu35, 1.0, silu35], rtol=0, atol=1e-14)
+    X2 = X.copy()
+    X2[0, [0, 2]] = 99.0
+    assert np.array_equal(oracle.tree_heads(X2, np.array([1]), W1, b1, W2, False)[1], z)
+
+
 def test_bf16_round_known_values():
     """Round-to-nearest-even at bf16's 8 significant bits: 1+2^-8 is a tie -> 1 (even),
     1+3*2^-8 is a tie -> 1+2^-6 (even), 1+2^-8+2^-30 -> 1+2^-7, sign symmetric."""
