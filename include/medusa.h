@@ -154,6 +154,34 @@ int medusa_heads_topk(const void* h, const void* w1, const void* b1, const void*
                       medusa_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * medusa_heads_topk_tree
+ * The Medusa heads over the hidden state of every tree node, of which each
+ * request keeps the top-k of its accepted node: the candidates of the next
+ * step come out of the verification pass with no separate pass over the
+ * accepted token (wiblog "Inference flow in an online chat service"; the
+ * accepted branch continues the sequence, Ultralytics "Tree attention and
+ * accepting tokens").  For node row x[b,i]: u_k = x + SiLU(W1_k x + b1_k),
+ * z_k = W2_k u_k, computed for all B*T rows (bf16 with B*T >= 3: both head
+ * products as tcgen05 GEMMs); request b keeps the top-k of row best_node[b].
+ *   x [B,T,H] (the tree nodes' hidden states, as given to
+ *   medusa_verify_accept); w1, b1, w2 as in medusa_heads_topk;
+ *   best_node [B] int32 device (medusa_verify_accept's output; values outside
+ *   [0, T) are clamped).
+ *   head_logits [B,K,V] fp32 or NULL: the logits of the accepted rows.
+ *   topk_ids, topk_vals [B,K,topk]: as medusa_heads_topk, ready for the next
+ *   step's medusa_build_tree together with medusa_verify_accept's next_root.
+ *   Limits as medusa_heads_topk.  The workspace holds the [B*T, K, V] logits of
+ *   every row (and the [B*T, K*H] first-layer outputs).
+ * ---------------------------------------------------------------------- */
+size_t medusa_heads_topk_tree_workspace_size(const medusa_tree* tree, int32_t B, int32_t H, int32_t V,
+                                             int32_t K, int32_t topk, medusa_dtype dtype);
+int medusa_heads_topk_tree(const medusa_tree* tree, const void* x, const void* w1, const void* b1,
+                           const void* w2, const int32_t* best_node, int32_t B, int32_t H, int32_t V,
+                           int32_t K, int32_t topk, medusa_dtype dtype, float* head_logits,
+                           int32_t* topk_ids, float* topk_vals, void* ws, size_t ws_bytes,
+                           medusa_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * medusa_heads_topk_noalloc
  * No counterpart on the source pages: a convenience of this library.
  * The computation, arguments and outputs of medusa_heads_topk, minus the

@@ -6,7 +6,8 @@ library raises ImportError: there is no CPU fallback.
 """
 from ._binding import (  # noqa: F401
     DEV_BAD_TOKEN, DEV_KV_OVERFLOW, DEV_NAN, DEV_TIMEOUT, MEDUSA_BF16, MEDUSA_F32, MedusaError, Tree, lib,
-    medusa_build_tree, medusa_heads_topk, medusa_heads_topk_workspace_size, kernel_launches, medusa_kv_commit,
+    medusa_build_tree, medusa_heads_topk, medusa_heads_topk_tree, medusa_heads_topk_tree_workspace_size,
+    medusa_heads_topk_workspace_size, kernel_launches, medusa_kv_commit,
     medusa_tree_attention, medusa_tree_attention_workspace_size, medusa_verify_accept,
     medusa_verify_accept_workspace_size, workspace,
 )

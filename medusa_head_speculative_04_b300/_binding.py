@@ -68,6 +68,9 @@ _sig("medusa_heads_topk", ctypes.c_int,
      [_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, ctypes.c_int, _vp, _vp, _vp, _vp, _vp, _sz, _vp])
 _sig("medusa_heads_topk_noalloc", ctypes.c_int,
      [_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, ctypes.c_int, _vp, _vp, _vp, _vp, _vp])
+_sig("medusa_heads_topk_tree_workspace_size", _sz, [_vp, _i32, _i32, _i32, _i32, _i32, ctypes.c_int])
+_sig("medusa_heads_topk_tree", ctypes.c_int,
+     [_vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, ctypes.c_int, _vp, _vp, _vp, _vp, _sz, _vp])
 _sig("medusa_build_tree", ctypes.c_int, [_vp, _vp, _vp, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _vp])
 _sig("medusa_tree_attention_workspace_size", _sz, [_vp, _i32, _i32, _i32, _i32, _i32, _i32, ctypes.c_int])
 _sig("medusa_tree_attention", ctypes.c_int,
@@ -191,6 +194,19 @@ def medusa_heads_topk_noalloc(h, w1, b1, w2, lm_head, topk: int, topk_ids, topk_
     _check("medusa_heads_topk_noalloc", lib.medusa_heads_topk_noalloc(
         _ptr(h), _ptr(w1), _ptr(b1), _ptr(w2), _ptr(lm_head), B, H, V, K, topk, dtype_code(h),
         _ptr(head_logits), _ptr(topk_ids), _ptr(topk_vals), _ptr(root_tok), _stream(stream)))
+
+
+def medusa_heads_topk_tree_workspace_size(tree: Tree, B, H, V, K, topk, dtype_c) -> int:
+    return lib.medusa_heads_topk_tree_workspace_size(tree.handle, B, H, V, K, topk, dtype_c)
+
+
+def medusa_heads_topk_tree(tree: Tree, x, w1, b1, w2, best_node, topk: int, topk_ids, topk_vals, ws,
+                           head_logits=None, stream=None) -> None:
+    B, T, H = x.shape
+    K, V = w2.shape[0], w2.shape[1]
+    _check("medusa_heads_topk_tree", lib.medusa_heads_topk_tree(
+        tree.handle, _ptr(x), _ptr(w1), _ptr(b1), _ptr(w2), _ptr(best_node), B, H, V, K, topk, dtype_code(x),
+        _ptr(head_logits), _ptr(topk_ids), _ptr(topk_vals), _ptr(ws), ws.numel(), _stream(stream)))
 
 
 def medusa_build_tree(tree: Tree, root_tok, topk_ids, kv_len, tree_tokens, position_ids,

@@ -18,6 +18,7 @@
 
 #include "gemv.cuh"
 #include "tc.cuh"
+#include "tree.cuh"
 
 using namespace medusa;
 
@@ -217,14 +218,17 @@ __global__ void __launch_bounds__(kThreads) heads_fc_act_kernel(const T* __restr
 // K2: CTA j of block blk holds rows [j*V/cph, (j+1)*V/cph) of that block.
 // Block blk < K is head blk (weights W2_blk, activations u[:, blk]); block K is
 // lm_head on h (root).  FROMZ: the logits were computed by the tensor-core GEMM
-// (zsrc [B, K, V]) and the CTA only selects from its slice of them.
+// (zsrc [rows, K, V]) and the CTA only selects from its slice of them; output
+// row b reads source row b, or row b * sel_T + row_sel[b] when row_sel is given
+// (device, read after the dependency wait), and copies it to head_logits when
+// that is given.
 template <typename T, int BMAX, bool FROMZ>
 __global__ void __launch_bounds__(kThreads) heads_vocab_kernel(
     const T* __restrict__ h, const T* __restrict__ u, const T* __restrict__ W2, const T* __restrict__ lm_head,
     int B, int b0, int nb, int H, int V, int K, int topk, int rpc, int cph,
     float* __restrict__ head_logits, int32_t* __restrict__ topk_ids, float* __restrict__ topk_vals,
     int32_t* __restrict__ root_tok, float* __restrict__ cand_v, int* __restrict__ cand_i, int* __restrict__ counters,
-    const float* __restrict__ zsrc) {
+    const float* __restrict__ zsrc, const int32_t* __restrict__ row_sel, int sel_T) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   const int blk = blockIdx.x / cph, cta = blockIdx.x % cph;
   const bool is_root = blk == K;
@@ -254,7 +258,11 @@ __global__ void __launch_bounds__(kThreads) heads_vocab_kernel(
   if (FROMZ) {
     for (int e = threadIdx.x; e < nb * n; e += blockDim.x) {
       const int b = e / n, lr = e % n;
-      zs[static_cast<size_t>(b) * rpc + lr] = zsrc[(static_cast<size_t>(b0 + b) * K + blk) * V + v0 + lr];
+      const size_t src = row_sel ? static_cast<size_t>(b0 + b) * sel_T + min(max(row_sel[b0 + b], 0), sel_T - 1)
+                                 : static_cast<size_t>(b0 + b);
+      const float z = zsrc[(src * K + blk) * V + v0 + lr];
+      zs[static_cast<size_t>(b) * rpc + lr] = z;
+      if (head_logits) head_logits[(static_cast<size_t>(b0 + b) * K + blk) * V + v0 + lr] = z;
     }
   } else {
     stage_rows(xs, x, x_stride, nb, H);
@@ -337,14 +345,14 @@ int launch_fc(const HeadsPlan& p, const HeadsWs& w, const T* h, const T* W1, con
 template <typename T, int BMAX, bool FROMZ>
 int launch_vocab(const HeadsPlan& p, const HeadsWs& w, const T* h, const T* W2, const T* lm, int B, int b0, int nb,
                  int H, int V, int K, int topk, float* head_logits, int32_t* topk_ids, float* topk_vals,
-                 int32_t* root_tok, const float* zsrc, cudaStream_t st) {
+                 int32_t* root_tok, const float* zsrc, const int32_t* row_sel, int sel_T, cudaStream_t st) {
   const size_t smem = vocab_smem_bytes(nb, BMAX, H, sizeof(T), p.rpc, p.cph, topk);
   auto vk = heads_vocab_kernel<T, BMAX, FROMZ>;
   if (!ensure_dyn_smem(vk, smem))
     return MEDUSA_ERR_CUDA;
   if (launch_pdl(vk, dim3(p.nblk * p.cph), dim3(kThreads), smem, st, h, static_cast<const T*>(w.u), W2, lm, B, b0, nb,
-                 H, V, K, topk, p.rpc, p.cph, FROMZ ? nullptr : head_logits, topk_ids, topk_vals, root_tok, w.cand_v,
-                 w.cand_i, w.counters, zsrc) != cudaSuccess) {
+                 H, V, K, topk, p.rpc, p.cph, head_logits, topk_ids, topk_vals, root_tok, w.cand_v, w.cand_i,
+                 w.counters, zsrc, row_sel, sel_T) != cudaSuccess) {
     (void)cudaGetLastError();
     return MEDUSA_ERR_CUDA;
   }
@@ -355,12 +363,12 @@ int launch_vocab(const HeadsPlan& p, const HeadsWs& w, const T* h, const T* W2, 
 template <typename T, bool FROMZ>
 int launch_vocab_nb(const HeadsPlan& p, const HeadsWs& w, const T* h, const T* W2, const T* lm, int B, int b0,
                     int nb, int H, int V, int K, int topk, float* hl, int32_t* ids, float* vals, int32_t* root,
-                    const float* zsrc, cudaStream_t st) {
-  if (nb == 1) return launch_vocab<T, 1, FROMZ>(p, w, h, W2, lm, B, b0, nb, H, V, K, topk, hl, ids, vals, root, zsrc, st);
-  if (nb == 2) return launch_vocab<T, 2, FROMZ>(p, w, h, W2, lm, B, b0, nb, H, V, K, topk, hl, ids, vals, root, zsrc, st);
-  if (nb <= 4) return launch_vocab<T, 4, FROMZ>(p, w, h, W2, lm, B, b0, nb, H, V, K, topk, hl, ids, vals, root, zsrc, st);
-  if (nb <= 8) return launch_vocab<T, 8, FROMZ>(p, w, h, W2, lm, B, b0, nb, H, V, K, topk, hl, ids, vals, root, zsrc, st);
-  return launch_vocab<T, 16, FROMZ>(p, w, h, W2, lm, B, b0, nb, H, V, K, topk, hl, ids, vals, root, zsrc, st);
+                    const float* zsrc, cudaStream_t st, const int32_t* row_sel = nullptr, int sel_T = 0) {
+  if (nb == 1) return launch_vocab<T, 1, FROMZ>(p, w, h, W2, lm, B, b0, nb, H, V, K, topk, hl, ids, vals, root, zsrc, row_sel, sel_T, st);
+  if (nb == 2) return launch_vocab<T, 2, FROMZ>(p, w, h, W2, lm, B, b0, nb, H, V, K, topk, hl, ids, vals, root, zsrc, row_sel, sel_T, st);
+  if (nb <= 4) return launch_vocab<T, 4, FROMZ>(p, w, h, W2, lm, B, b0, nb, H, V, K, topk, hl, ids, vals, root, zsrc, row_sel, sel_T, st);
+  if (nb <= 8) return launch_vocab<T, 8, FROMZ>(p, w, h, W2, lm, B, b0, nb, H, V, K, topk, hl, ids, vals, root, zsrc, row_sel, sel_T, st);
+  return launch_vocab<T, 16, FROMZ>(p, w, h, W2, lm, B, b0, nb, H, V, K, topk, hl, ids, vals, root, zsrc, row_sel, sel_T, st);
 }
 
 template <typename T>
@@ -405,8 +413,8 @@ int heads_dispatch(const HeadsPlan& p, const HeadsWs& w, const T* h, const T* W1
     int rc = tc_heads(w, h, W1, b1, W2, B, H, V, K, z, st);
     if (rc != MEDUSA_OK) return rc;
     for (int b0 = 0; b0 < B; b0 += p.bgroup) {
-      rc = launch_vocab_nb<T, true>(p, w, h, W2, lm, B, b0, std::min(p.bgroup, B - b0), H, V, K, topk, hl, ids, vals,
-                                    root, z, st);
+      rc = launch_vocab_nb<T, true>(p, w, h, W2, lm, B, b0, std::min(p.bgroup, B - b0), H, V, K, topk, nullptr, ids,
+                                    vals, root, z, st);
       if (rc != MEDUSA_OK) return rc;
     }
     return MEDUSA_OK;
@@ -460,6 +468,139 @@ MEDUSA_API int medusa_heads_topk(const void* h, const void* w1, const void* b1, 
                         static_cast<const float*>(b1), static_cast<const float*>(w2),
                         static_cast<const float*>(lm_head), B, H, V, K, topk, head_logits, topk_ids, topk_vals,
                         root_tok, st);
+}
+
+// ---------------------------------------------------------------------------
+// medusa_heads_topk_tree: the heads over the hidden state of every tree node
+// (rows b*T + i of x), of which each request keeps the top-k of its accepted
+// node for the next step.  wiblog.cn "Medusa multi-head speculative decoding",
+// section "Inference flow in an online chat service": the verification pass
+// that scores the candidates also yields what the next round's candidates come
+// from, with no extra forward pass; Ultralytics glossary "Medusa Heads",
+// section "Tree attention and accepting tokens": the accepted branch continues
+// the sequence.  The rows' count B*T makes both head products dense GEMMs
+// (bf16: the tcgen05 path), and the top-k runs only on the accepted rows.
+// ---------------------------------------------------------------------------
+namespace {
+
+// CUDA-core path: request b's top-k (and logits) copied from row b*T + best[b].
+__global__ void __launch_bounds__(256) gather_topk_kernel(const int32_t* __restrict__ ids_all,
+                                                          const float* __restrict__ vals_all,
+                                                          const float* __restrict__ logits_all,
+                                                          const int32_t* __restrict__ best, int T, int K, int topk,
+                                                          int V, int32_t* __restrict__ ids, float* __restrict__ vals,
+                                                          float* __restrict__ logits) {
+  const int b = blockIdx.x;
+  pdl_wait();
+  pdl_trigger();
+  const int node = min(max(best[b], 0), T - 1);
+  const size_t src = static_cast<size_t>(b) * T + node;
+  const int nk = K * topk;
+  for (int e = threadIdx.x; e < nk; e += blockDim.x) {
+    ids[static_cast<size_t>(b) * nk + e] = ids_all[src * nk + e];
+    vals[static_cast<size_t>(b) * nk + e] = vals_all[src * nk + e];
+  }
+  if (logits) {
+    const size_t nv = static_cast<size_t>(K) * V;
+    for (size_t e = threadIdx.x; e < nv; e += blockDim.x) logits[b * nv + e] = logits_all[src * nv + e];
+  }
+}
+
+struct TreeHeadsWs {
+  HeadsWs hw;
+  int32_t* ids_all;    // CUDA-core path: [B*T, K, topk]
+  float* vals_all;
+  float* logits_all;   // CUDA-core path: [B*T, K, V]
+  size_t bytes;
+};
+
+TreeHeadsWs carve_tree_heads_ws(void* base, const HeadsPlan& p, int R, int H, int V, int K, int topk, int es) {
+  TreeHeadsWs w{};
+  w.hw = carve_heads_ws(base, p, R, H, V, K, topk, es);
+  size_t o = w.hw.bytes;
+  auto take = [&](size_t n) { size_t s = o; o = align_up(o + n, 256); return s; };
+  const size_t nk = static_cast<size_t>(R) * K * topk;
+  const size_t oi = p.tc ? 0 : take(nk * 4), ov = p.tc ? 0 : take(nk * 4);
+  const size_t ol = p.tc ? 0 : take(static_cast<size_t>(R) * K * V * 4);
+  char* c = static_cast<char*>(base);
+  if (c && !p.tc) {
+    w.ids_all = reinterpret_cast<int32_t*>(c + oi);
+    w.vals_all = reinterpret_cast<float*>(c + ov);
+    w.logits_all = reinterpret_cast<float*>(c + ol);
+  }
+  w.bytes = o;
+  return w;
+}
+
+template <typename T>
+int tree_heads_dispatch(const HeadsPlan& p, const TreeHeadsWs& w, const T* x, const T* W1, const T* b1, const T* W2,
+                        const int32_t* best, int B, int Tn, int H, int V, int K, int topk, float* hl, int32_t* ids,
+                        float* vals, cudaStream_t st) {
+  const int R = B * Tn;
+  if (p.tc) {
+    // u and z = W2_k u_k for every row on the tensor cores, then the accepted rows' top-k
+    int rc = tc_heads(w.hw, x, W1, b1, W2, R, H, V, K, w.hw.z, st);
+    if (rc != MEDUSA_OK) return rc;
+    for (int b0 = 0; b0 < B; b0 += p.bgroup) {
+      rc = launch_vocab_nb<T, true>(p, w.hw, x, W2, static_cast<const T*>(nullptr), B, b0, std::min(p.bgroup, B - b0),
+                                    H, V, K, topk, hl, ids, vals, nullptr, w.hw.z, st, best, Tn);
+      if (rc != MEDUSA_OK) return rc;
+    }
+    return MEDUSA_OK;
+  }
+  int rc = heads_dispatch(p, w.hw, x, W1, b1, W2, static_cast<const T*>(nullptr), R, H, V, K, topk, w.logits_all,
+                          w.ids_all, w.vals_all, nullptr, st);
+  if (rc != MEDUSA_OK) return rc;
+  if (launch_pdl(gather_topk_kernel, dim3(B), dim3(256), 0, st, static_cast<const int32_t*>(w.ids_all),
+                 static_cast<const float*>(w.vals_all), static_cast<const float*>(w.logits_all), best, Tn, K, topk, V,
+                 ids, vals, hl) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return MEDUSA_ERR_CUDA;
+  }
+  MEDUSA_LAUNCH_CHECK();
+  return MEDUSA_OK;
+}
+
+}  // namespace
+
+MEDUSA_API size_t medusa_heads_topk_tree_workspace_size(const medusa_tree* tree, int32_t B, int32_t H, int32_t V,
+                                                        int32_t K, int32_t topk, medusa_dtype dtype) {
+  if (!tree || B < 1 || H < 8 || V < 1 || K < 1 || topk < 1) return 0;
+  const int es = dtype == MEDUSA_BF16 ? 2 : 4;
+  const int R = B * tree->T;
+  HeadsPlan p;
+  if (!plan_heads(R, H, V, K, 0, es, topk, true, &p)) return 0;
+  return carve_tree_heads_ws(nullptr, p, R, H, V, K, topk, es).bytes;
+}
+
+MEDUSA_API int medusa_heads_topk_tree(const medusa_tree* tree, const void* x, const void* w1, const void* b1,
+                                      const void* w2, const int32_t* best_node, int32_t B, int32_t H, int32_t V,
+                                      int32_t K, int32_t topk, medusa_dtype dtype, float* head_logits,
+                                      int32_t* topk_ids, float* topk_vals, void* ws, size_t ws_bytes,
+                                      medusa_stream_t stream) {
+  if (!tree || !x || !w1 || !b1 || !w2 || !best_node || !topk_ids || !topk_vals) return MEDUSA_ERR_INVALID_ARG;
+  if (dtype != MEDUSA_F32 && dtype != MEDUSA_BF16) return MEDUSA_ERR_INVALID_ARG;
+  if (B < 1 || B > MEDUSA_MAX_BATCH || K < 1 || V < 1 || H < 8 || topk < 1 || topk > MEDUSA_MAX_TOPK || topk > V)
+    return MEDUSA_ERR_INVALID_ARG;
+  if (H % 8 != 0) return MEDUSA_ERR_UNSUPPORTED;
+  const void* ptrs[] = {x, w1, b1, w2, best_node, topk_ids, topk_vals};
+  for (const void* q : ptrs)
+    if (!aligned16(q)) return MEDUSA_ERR_ALIGNMENT;
+  if ((head_logits && !aligned16(head_logits)) || (ws && !aligned16(ws))) return MEDUSA_ERR_ALIGNMENT;
+  const int es = dtype == MEDUSA_BF16 ? 2 : 4;
+  const int Tn = tree->T, R = B * Tn;
+  HeadsPlan p;
+  if (!plan_heads(R, H, V, K, 0, es, topk, true, &p)) return MEDUSA_ERR_UNSUPPORTED;
+  TreeHeadsWs w = carve_tree_heads_ws(ws, p, R, H, V, K, topk, es);
+  if (!ws || ws_bytes < w.bytes) return MEDUSA_ERR_WORKSPACE;
+  auto st = reinterpret_cast<cudaStream_t>(stream);
+  if (dtype == MEDUSA_BF16)
+    return tree_heads_dispatch(p, w, static_cast<const __nv_bfloat16*>(x), static_cast<const __nv_bfloat16*>(w1),
+                               static_cast<const __nv_bfloat16*>(b1), static_cast<const __nv_bfloat16*>(w2), best_node,
+                               B, Tn, H, V, K, topk, head_logits, topk_ids, topk_vals, st);
+  return tree_heads_dispatch(p, w, static_cast<const float*>(x), static_cast<const float*>(w1),
+                             static_cast<const float*>(b1), static_cast<const float*>(w2), best_node, B, Tn, H, V, K,
+                             topk, head_logits, topk_ids, topk_vals, st);
 }
 
 // ---------------------------------------------------------------------------

@@ -62,6 +62,7 @@ class MedusaStep:
         self.ws_attn = mb.workspace(mb.medusa_tree_attention_workspace_size(self.tree, B, Hq, Hkv, D, Lmax,
                                                                             kv_len_hint, dc), self.device)
         self.ws_verify = mb.workspace(mb.medusa_verify_accept_workspace_size(self.tree, B, H, V, dc), self.device)
+        self.ws_tree_heads = None  # allocated on the first heads_from_tree call
 
     @property
     def T(self) -> int:
@@ -71,6 +72,19 @@ class MedusaStep:
         mb.medusa_heads_topk(h, W1, b1, W2, lm_head if self.root_from_lm_head else None, self.topk,
                              self.topk_ids, self.topk_vals, self.root, self.ws_heads,
                              head_logits=self.head_logits, stream=stream)
+
+    def heads_from_tree(self, X, W1, b1, W2, stream=None):
+        """Next step's candidates from the heads over every tree node's state X (the
+        verification input): the top-k of each request's accepted node go to
+        ``topk_ids``/``topk_vals`` and its next token to ``root``, so the next
+        :meth:`build` continues from the accepted branch."""
+        if self.ws_tree_heads is None:
+            dc = mb.MEDUSA_BF16 if self.dtype == torch.bfloat16 else mb.MEDUSA_F32
+            self.ws_tree_heads = mb.workspace(mb.medusa_heads_topk_tree_workspace_size(
+                self.tree, self.B, self.H, self.V, self.K, self.topk, dc), self.device)
+        mb.medusa_heads_topk_tree(self.tree, X, W1, b1, W2, self.best_node, self.topk, self.topk_ids,
+                                  self.topk_vals, self.ws_tree_heads, head_logits=self.head_logits, stream=stream)
+        self.root.copy_(self.next_root)
 
     def build(self, kv_len, root=None, stream=None):
         mb.medusa_build_tree(self.tree, self.root if root is None else root, self.topk_ids, kv_len, self.tokens,
