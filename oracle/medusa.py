@@ -336,7 +336,7 @@ def node_posterior(z_parent: np.ndarray, token: int, temperature: float,
 
 
 def typical_accept(z: np.ndarray, tokens: np.ndarray, tt: TreeTables, temperature: float,
-                   threshold: float, alpha: float) -> Dict[str, np.ndarray]:
+                   threshold: float, alpha: float, tie_break: str = "first") -> Dict[str, np.ndarray]:
     """Longest accepted prefix of the candidate tree, per request.
 
     A node is kept when its own token passes the acceptance test under its
@@ -347,7 +347,11 @@ def typical_accept(z: np.ndarray, tokens: np.ndarray, tt: TreeTables, temperatur
 
     Reading: accept_length counts the tokens accepted beyond the root, i.e.
     the depth of the deepest kept node; among equally deep kept nodes the one
-    first in canonical order wins (higher-ranked head candidates first);
+    first in canonical order wins (higher-ranked head candidates first), or,
+    with tie_break="joint", the one whose path has the highest joint
+    probability (the product of each node's p under its parent; the pages
+    leave the choice open), equal products again to the first in canonical
+    order;
     best_path is the first path (leaf in canonical order) through that node;
     the next root is the greedy token of the winner's logits [WIB "Inference
     flow": the next round starts from the last accepted token].
@@ -355,7 +359,7 @@ def typical_accept(z: np.ndarray, tokens: np.ndarray, tt: TreeTables, temperatur
     """
     B, T = tokens.shape
     out = {k: [] for k in ("accept_len", "best_node", "best_path", "accepted_tokens",
-                           "next_root", "node_p", "node_H", "node_accept", "margin")}
+                           "next_root", "node_p", "node_H", "node_accept", "margin", "joint_margin")}
     dmax = tt.dmax
     for b in range(B):
         p = np.full(T, np.nan)
@@ -373,6 +377,18 @@ def typical_accept(z: np.ndarray, tokens: np.ndarray, tt: TreeTables, temperatur
         for c in range(1, T):
             if kept[c] and tt.depth[c] > tt.depth[best]:
                 best = c
+        joint_margin = np.inf
+        if tie_break == "joint":
+            # log joint probability of each kept node's path (root: ln 1 = 0)
+            lp = np.zeros(T)
+            for c in range(1, T):
+                lp[c] = lp[tt.parent[c]] + (np.log(p[c]) if p[c] > 0 else -np.inf)
+            deepest = [c for c in range(T) if kept[c] and tt.depth[c] == tt.depth[best]]
+            best = max(deepest, key=lambda c: (lp[c], -c))
+            others = [abs(lp[c] - lp[best]) for c in deepest if c != best]
+            joint_margin = min(others) if others else np.inf
+        elif tie_break != "first":
+            raise ValueError(tie_break)
         a = int(tt.depth[best])
         chain = tt.ancestors[best] + [best]
         bp = next(pi for pi, leaf in enumerate(tt.leaves) if best == leaf or best in tt.ancestors[leaf])
@@ -387,6 +403,7 @@ def typical_accept(z: np.ndarray, tokens: np.ndarray, tt: TreeTables, temperatur
         out["node_H"].append(H)
         out["node_accept"].append(kept)
         out["margin"].append(margin)
+        out["joint_margin"].append(joint_margin)
     return {k: np.array(v) for k, v in out.items()}
 
 

@@ -427,6 +427,36 @@ def test_longest_prefix_and_tie_break():
 
 # --------------------------------------------------------------------------- commit
 
+def test_joint_probability_tie_break_hand_example():
+    """Among equally deep kept nodes, the tie-break by highest joint probability (the
+    product of each node's p under its parent) against first-in-canonical-order, on a
+    hand-built 2 x 3 tree at temperature 1.  Tokens: root 0, depth 1 (0,)->1, (1,)->2,
+    depth 2 ranks 0,1,2 -> tokens 3,4,5 under both.  exp(logits): root [1,3,1,1,1,1]
+    (p(1) = 3/8, p(2) = 1/8, H = 1.6675, threshold 0.0566: both kept); node (0,)
+    [1,1,1,2,1,1] (2/7, 1/7, 1/7 against 0.0522: all kept); node (1,) [1,1,1,1,1,40]
+    (1/45, 1/45, 40/45 against min(0.09, 0.177) = 0.09: only (1,2) kept).  Joint
+    probabilities of the depth-2 survivors: (0,0) 3/8 * 2/7 = 0.1071, (0,1) = (0,2) =
+    0.0536, (1,2) 1/8 * 40/45 = 0.1111.  First-in-order picks (0,0), node 3; joint picks
+    (1,2), node 8."""
+    tt = oracle.tree_tables(synth.cartesian_choices((2, 3)))
+    assert tt.nodes[3] == (0, 0) and tt.nodes[8] == (1, 2)
+    tokens = np.array([[0, 1, 2, 3, 4, 5, 3, 4, 5]])
+    z = np.zeros((1, tt.T, 6))
+    z[0, 0] = np.log([1, 3, 1, 1, 1, 1])
+    z[0, 1] = np.log([1, 1, 1, 2, 1, 1])
+    z[0, 2] = np.log([1, 1, 1, 1, 1, 40])
+    first = oracle.typical_accept(z, tokens, tt, 1.0, 0.09, 0.3)
+    joint = oracle.typical_accept(z, tokens, tt, 1.0, 0.09, 0.3, tie_break="joint")
+    assert first["accept_len"][0] == joint["accept_len"][0] == 2
+    assert first["best_node"][0] == 3 and joint["best_node"][0] == 8
+    assert joint["accepted_tokens"][0].tolist() == [0, 2, 5]
+    assert abs(joint["joint_margin"][0] - (math.log(40 / 360) - math.log(6 / 56))) < 1e-12
+    # at temperature 0 every kept node has p = 1: the joint rule falls back to the order
+    g0 = oracle.typical_accept(z, tokens, tt, 0.0, 0.09, 0.3, tie_break="joint")
+    f0 = oracle.typical_accept(z, tokens, tt, 0.0, 0.09, 0.3)
+    assert g0["best_node"][0] == f0["best_node"][0]
+
+
 def test_kv_commit_rows_and_overflow():
     tt = oracle.tree_tables(synth.cartesian_choices((2, 3)))
     r = _rng(7)
