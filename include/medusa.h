@@ -288,7 +288,11 @@ int medusa_tree_attention(const medusa_tree* tree, const void* q, const void* k_
  *     posterior_alpha * exp(-H)).
  *   A node is kept iff it is accepted and its parent is kept; the root is
  *   always kept (the first token is the greedy one).  The deepest kept node
- *   wins, ties to the first in canonical order.
+ *   wins; among equally deep kept nodes (the pages leave the choice open):
+ *     tie_break 0: the first in canonical order (higher-ranked candidates);
+ *     tie_break 1: the one whose path has the highest joint probability (the
+ *       product of each node's p under its parent), equal products to the
+ *       first in canonical order (at temperature 0 every kept p is 1).
  * Outputs (device):
  *   logits [B,T,V] fp32 or NULL; node_p [B,T] or NULL (p of node c under its
  *   parent; 1/0 = match/miss at temperature 0; 1 for the root); node_H [B,T]
@@ -305,7 +309,7 @@ size_t medusa_verify_accept_workspace_size(const medusa_tree* tree, int32_t B, i
 int medusa_verify_accept(const medusa_tree* tree, const void* x, const void* lm_head,
                          const int32_t* tree_tokens, int32_t B, int32_t H, int32_t V,
                          medusa_dtype dtype, float temperature, float posterior_threshold,
-                         float posterior_alpha, float* logits, float* node_p, float* node_H,
+                         float posterior_alpha, int32_t tie_break, float* logits, float* node_p, float* node_H,
                          int32_t* accept_len, int32_t* best_path, int32_t* best_node,
                          int32_t* accepted_tokens, int32_t* next_root, int32_t* dev_status,
                          void* ws, size_t ws_bytes, medusa_stream_t stream);

@@ -79,8 +79,8 @@ _sig("medusa_tree_attention", ctypes.c_int,
 _sig("medusa_tree_query", ctypes.c_int, [_vp, _vp, _vp, _vp, _vp])
 _sig("medusa_verify_accept_workspace_size", _sz, [_vp, _i32, _i32, _i32, ctypes.c_int])
 _sig("medusa_verify_accept", ctypes.c_int,
-     [_vp, _vp, _vp, _vp, _i32, _i32, _i32, ctypes.c_int, _f32, _f32, _f32, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
-      _vp, _vp, _vp, _sz, _vp])
+     [_vp, _vp, _vp, _vp, _i32, _i32, _i32, ctypes.c_int, _f32, _f32, _f32, _i32, _vp, _vp, _vp, _vp, _vp, _vp,
+      _vp, _vp, _vp, _vp, _sz, _vp])
 _sig("medusa_kv_commit", ctypes.c_int,
      [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, ctypes.c_int, _vp, _vp])
 
@@ -239,12 +239,14 @@ def medusa_verify_accept_workspace_size(tree: Tree, B, H, V, dtype_c) -> int:
 
 def medusa_verify_accept(tree: Tree, x, lm_head, tree_tokens, temperature: float, posterior_threshold: float,
                          posterior_alpha: float, accept_len, best_path, best_node, accepted_tokens, next_root,
-                         ws, logits=None, node_p=None, node_H=None, dev_status=None, stream=None) -> None:
+                         ws, logits=None, node_p=None, node_H=None, dev_status=None, stream=None,
+                         tie_break: str = "first") -> None:
     B, T, H = x.shape
     V = lm_head.shape[0]
+    tb = {"first": 0, "joint": 1}[tie_break]
     _check("medusa_verify_accept", lib.medusa_verify_accept(
         tree.handle, _ptr(x), _ptr(lm_head), _ptr(tree_tokens), B, H, V, dtype_code(x), temperature,
-        posterior_threshold, posterior_alpha, _ptr(logits), _ptr(node_p), _ptr(node_H), _ptr(accept_len),
+        posterior_threshold, posterior_alpha, tb, _ptr(logits), _ptr(node_p), _ptr(node_H), _ptr(accept_len),
         _ptr(best_path), _ptr(best_node), _ptr(accepted_tokens), _ptr(next_root), _ptr(dev_status), _ptr(ws),
         ws.numel(), _stream(stream)))
 

@@ -139,6 +139,7 @@ struct VerifyWs {
   float* child_z;    // [R] logit of node c's token under its parent (indexed by c)
   float4* rowst;     // [R] merged statistics
   unsigned char* acc;  // [R] each node's acceptance test against its parent
+  float* logp;       // [R] ln p of each node under its parent (joint-probability tie-break)
   int* tickets;      // [B] CTAs done with a request's nodes (self-resetting)
   float* zbuf;       // fp32 path: [R, V] logits when the caller gives none
   size_t bytes;
@@ -150,7 +151,7 @@ VerifyWs carve_verify_ws(void* base, const VerifyPlan& p, int V, medusa_dtype dt
   auto take = [&](size_t n) { size_t s = o; o = align_up(o + n, 256); return s; };
   size_t op = take(static_cast<size_t>(p.R) * p.n_parts * 16), oc = take(static_cast<size_t>(p.R) * 4),
          orow = take(static_cast<size_t>(p.R) * 16), otk = take(static_cast<size_t>(p.R) * 4),
-         oa = take(static_cast<size_t>(p.R));
+         oa = take(static_cast<size_t>(p.R)), olp = take(static_cast<size_t>(p.R) * 4);
   size_t oz = dt == MEDUSA_F32 ? take(static_cast<size_t>(p.R) * V * 4) : 0;
   char* c = static_cast<char*>(base);
   if (c) {
@@ -159,6 +160,7 @@ VerifyWs carve_verify_ws(void* base, const VerifyPlan& p, int V, medusa_dtype dt
     w.rowst = reinterpret_cast<float4*>(c + orow);
     w.tickets = reinterpret_cast<int*>(c + otk);
     w.acc = reinterpret_cast<unsigned char*>(c + oa);
+    w.logp = reinterpret_cast<float*>(c + olp);
     w.zbuf = dt == MEDUSA_F32 ? reinterpret_cast<float*>(c + oz) : nullptr;
   }
   w.bytes = o;
@@ -707,6 +709,8 @@ struct AcceptArgs {
   int n_nt, R;
   float4* rowst;       // [R] merged statistics
   unsigned char* acc;  // [R] typical-acceptance test of each node against its parent (root: 1)
+  float* logp;         // [R] ln p of each node under its parent (root: 0)
+  int joint;           // tie-break among the deepest kept nodes: 0 first in order, 1 highest joint probability
   int* tickets;        // [B] self-resetting
   const float* child_z;
   float inv_tau, thr, alpha;
@@ -726,26 +730,43 @@ struct AcceptArgs {
 // A node is kept when it and all its ancestors passed; the deepest kept node
 // wins, ties to the lowest canonical index.
 // ------------------------------------------------------------------------
+__device__ inline uint32_t ordered_bits(float f) {  // monotone map of floats to unsigned (NaN lowest)
+  if (f != f) return 0u;
+  const uint32_t u = __float_as_uint(f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
 __device__ void accept_request(const AcceptArgs& a, int b, unsigned char* s_acc, const int16_t* s_par,
-                               const int16_t* s_dep, const int16_t* s_fp, int* s_chain, int* s_best) {
+                               const int16_t* s_dep, const int16_t* s_fp, float* s_lp, int* s_chain,
+                               unsigned long long* s_best) {
   const medusa_tree_dev& tr = a.tr;
   const int T = tr.T;
   const size_t base = static_cast<size_t>(b) * T;
-  if (threadIdx.x == 0) *s_best = 0;
-  for (int c = threadIdx.x; c < T; c += blockDim.x) s_acc[c] = __ldcg(a.acc + base + c);
+  if (threadIdx.x == 0) *s_best = 0ull;
+  for (int c = threadIdx.x; c < T; c += blockDim.x) {
+    s_acc[c] = __ldcg(a.acc + base + c);
+    if (a.joint) s_lp[c] = c == 0 ? 0.f : __ldcg(a.logp + base + c);
+  }
   __syncthreads();
   for (int d = 1; d <= tr.dmax; ++d) {
     for (int c = threadIdx.x; c < T; c += blockDim.x)
-      if (s_dep[c] == d) s_acc[c] = s_acc[c] && s_acc[s_par[c]];
+      if (s_dep[c] == d) {
+        s_acc[c] = s_acc[c] && s_acc[s_par[c]];
+        if (a.joint) s_lp[c] += s_lp[s_par[c]];  // ln of the path's joint probability
+      }
     __syncthreads();
   }
-  int key = 0xFFFF;  // root: depth 0, index 0
+  // key: depth, then (joint rule) the path's log probability, then the lowest index
+  unsigned long long key = 0xFFFFull;  // root: depth 0, index 0
   for (int c = threadIdx.x; c < T; c += blockDim.x)
-    if (s_acc[c]) key = max(key, (static_cast<int>(s_dep[c]) << 16) | (0xFFFF - c));
+    if (s_acc[c]) {
+      const unsigned long long lp = a.joint ? ordered_bits(s_lp[c]) : 0u;
+      key = max(key, (static_cast<unsigned long long>(s_dep[c]) << 48) | (lp << 16) | (0xFFFFu - c));
+    }
   for (int o = 16; o > 0; o >>= 1) key = max(key, __shfl_xor_sync(0xffffffffu, key, o));
   if ((threadIdx.x & 31) == 0) atomicMax(s_best, key);
   __syncthreads();
-  const int best = 0xFFFF - (*s_best & 0xFFFF);
+  const int best = 0xFFFF - static_cast<int>(*s_best & 0xFFFFull);
   const int a_len = s_dep[best];
   if (threadIdx.x == 0) {
     int node = best;
@@ -785,9 +806,10 @@ __global__ void __launch_bounds__(kMergeRows * 32) merge_accept_kernel(AcceptArg
   int16_t* s_par = reinterpret_cast<int16_t*>(accept_smem);
   int16_t* s_dep = s_par + T;
   int16_t* s_fp = s_dep + T;
-  unsigned char* s_acc = reinterpret_cast<unsigned char*>(s_fp + T);
+  float* s_lp = reinterpret_cast<float*>(s_fp + T + (T & 1));  // 4-byte aligned after three int16 arrays
+  unsigned char* s_acc = reinterpret_cast<unsigned char*>(s_lp + T);
   __shared__ int s_chain[MEDUSA_MAX_DEPTH + 1];
-  __shared__ int s_best;
+  __shared__ unsigned long long s_best;
   __shared__ int s_last;
   for (int c = threadIdx.x; c < T; c += blockDim.x) {
     s_par[c] = static_cast<int16_t>(a.tr.parent[c]);
@@ -842,6 +864,7 @@ __global__ void __launch_bounds__(kMergeRows * 32) merge_accept_kernel(AcceptArg
         p = pass ? 1.f : 0.f;
       }
       a.acc[base + c_beg + k] = pass ? 1 : 0;
+      if (a.joint) a.logp[base + c_beg + k] = logf(p);
       if (a.node_p) a.node_p[base + c_beg + k] = p;
     }
   }
@@ -853,7 +876,7 @@ __global__ void __launch_bounds__(kMergeRows * 32) merge_accept_kernel(AcceptArg
     __syncthreads();
     if (s_last) {
       __threadfence();
-      accept_request(a, b, s_acc, s_par, s_dep, s_fp, s_chain, &s_best);
+      accept_request(a, b, s_acc, s_par, s_dep, s_fp, s_lp, s_chain, &s_best);
       if (threadIdx.x == 0) a.tickets[b] = 0;  // ready for the next launch
     }
     __syncthreads();
@@ -942,7 +965,7 @@ MEDUSA_API size_t medusa_verify_accept_workspace_size(const medusa_tree* tree, i
 MEDUSA_API int medusa_verify_accept(const medusa_tree* tree, const void* x, const void* lm_head,
                                     const int32_t* tree_tokens, int32_t B, int32_t H, int32_t V, medusa_dtype dtype,
                                     float temperature, float posterior_threshold, float posterior_alpha,
-                                    float* logits, float* node_p, float* node_H, int32_t* accept_len,
+                                    int32_t tie_break, float* logits, float* node_p, float* node_H, int32_t* accept_len,
                                     int32_t* best_path, int32_t* best_node, int32_t* accepted_tokens,
                                     int32_t* next_root, int32_t* dev_status, void* ws, size_t ws_bytes,
                                     medusa_stream_t stream) {
@@ -950,6 +973,7 @@ MEDUSA_API int medusa_verify_accept(const medusa_tree* tree, const void* x, cons
       !next_root)
     return MEDUSA_ERR_INVALID_ARG;
   if (B < 1 || B > MEDUSA_MAX_BATCH || H < 8 || V < 1 || !(temperature >= 0.f)) return MEDUSA_ERR_INVALID_ARG;
+  if (tie_break != 0 && tie_break != 1) return MEDUSA_ERR_INVALID_ARG;
   if (dtype != MEDUSA_F32 && dtype != MEDUSA_BF16) return MEDUSA_ERR_INVALID_ARG;
   if (H % 8 != 0) return MEDUSA_ERR_UNSUPPORTED;
   const void* ptrs[] = {x, lm_head, tree_tokens, accept_len, best_path, best_node, accepted_tokens, next_root};
@@ -1000,11 +1024,12 @@ MEDUSA_API int medusa_verify_accept(const medusa_tree* tree, const void* x, cons
     }
     MEDUSA_LAUNCH_CHECK();
   }
-  AcceptArgs aa{tree->dev, tree_tokens, w.part, p.n_parts, p.R, w.rowst, w.acc, w.tickets, w.child_z, inv_tau,
-                posterior_threshold, posterior_alpha, node_p, node_H, accept_len, best_path, best_node,
-                accepted_tokens, next_root, dev_status};
-  if (launch_pdl(merge_accept_kernel, dim3(cdiv(p.R, kMergeRows)), dim3(kMergeRows * 32), static_cast<size_t>(T) * 7,
-                 st, aa) != cudaSuccess) {
+  AcceptArgs aa{tree->dev, tree_tokens, w.part, p.n_parts, p.R, w.rowst, w.acc, w.logp, tie_break, w.tickets,
+                w.child_z, inv_tau, posterior_threshold, posterior_alpha, node_p, node_H, accept_len, best_path,
+                best_node, accepted_tokens, next_root, dev_status};
+  const size_t accept_smem = static_cast<size_t>(T) * 6 + (T & 1) * 2 + static_cast<size_t>(T) * 5;
+  if (launch_pdl(merge_accept_kernel, dim3(cdiv(p.R, kMergeRows)), dim3(kMergeRows * 32), accept_smem, st, aa) !=
+      cudaSuccess) {
     (void)cudaGetLastError();
     return MEDUSA_ERR_CUDA;
   }

@@ -21,7 +21,7 @@ class MedusaStep:
     def __init__(self, choices: Sequence[Sequence[int]], B: int, H: int, V: int, K: int, Hq: int, Hkv: int,
                  D: int, Lmax: int, topk: int, dtype: torch.dtype, device="cuda", root_from_lm_head=False,
                  kv_len_hint: int = 0, keep_head_logits=False, keep_logits=False, keep_node_stats=True,
-                 rope: bool = False, rope_theta: float = 10000.0):
+                 rope: bool = False, rope_theta: float = 10000.0, tie_break: str = "first"):
         self.tree = mb.Tree(choices)
         self.B, self.H, self.V, self.K = B, H, V, K
         self.Hq, self.Hkv, self.D, self.Lmax, self.topk = Hq, Hkv, D, Lmax, topk
@@ -31,6 +31,7 @@ class MedusaStep:
         # rope: the tree's q and k are rotated at the position ids the tree expansion
         # produced, and the rotated keys are what the commit appends to the cache
         self.rope, self.rope_theta = rope, rope_theta
+        self.tie_break = tie_break  # among equally deep accepted nodes: "first" in order or "joint" probability
         T, P, W = self.tree.T, self.tree.P, self.tree.dmax + 1
         dc = mb.MEDUSA_BF16 if dtype == torch.bfloat16 else mb.MEDUSA_F32
         i32 = dict(dtype=torch.int32, device=self.device)
@@ -100,7 +101,8 @@ class MedusaStep:
         mb.medusa_verify_accept(self.tree, X, lm_head, self.tokens, temperature, threshold, alpha,
                                 self.accept_len, self.best_path, self.best_node, self.accepted_tokens,
                                 self.next_root, self.ws_verify, logits=self.logits, node_p=self.node_p,
-                                node_H=self.node_H, dev_status=self.dev_status, stream=stream)
+                                node_H=self.node_H, dev_status=self.dev_status, stream=stream,
+                                tie_break=self.tie_break)
 
     def commit(self, k_new, v_new, k_cache, v_cache, kv_len, stream=None):
         mb.medusa_kv_commit(self.tree, self.k_rot if self.rope else k_new, v_new, k_cache, v_cache, kv_len,

@@ -73,10 +73,10 @@ def step_oracle_inputs(inp):
                                                "k_cache", "v_cache") if getattr(inp, k) is not None}
 
 
-def accept_parity(step, z_o, tokens_g, tt, temperature, thr, alpha, delta, kind):
+def accept_parity(step, z_o, tokens_g, tt, temperature, thr, alpha, delta, kind, tie_break="first"):
     """Compare the GPU acceptance outputs with the oracle's on the GPU's tree tokens.
     Returns the number of near-tie decisions (outputs may then differ)."""
-    acc = oracle.typical_accept(z_o, tokens_g, tt, temperature, thr, alpha)
+    acc = oracle.typical_accept(z_o, tokens_g, tt, temperature, thr, alpha, tie_break=tie_break)
     B = tokens_g.shape[0]
     near = 0
     tol = TOL[kind]
@@ -86,6 +86,7 @@ def accept_parity(step, z_o, tokens_g, tt, temperature, thr, alpha, delta, kind)
             tie = np.any(margins < delta * np.maximum(1.0, np.abs(z_o[b]).max()))
         else:
             tie = np.any(margins < delta / temperature)
+        tie = tie or acc["joint_margin"][b] < delta
         same = (int(step.accept_len[b]) == acc["accept_len"][b] and int(step.best_node[b]) == acc["best_node"][b]
                 and int(step.best_path[b]) == acc["best_path"][b]
                 and npi(step.accepted_tokens[b]).tolist() == acc["accepted_tokens"][b].tolist())

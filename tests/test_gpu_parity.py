@@ -42,7 +42,7 @@ def run_step(mb, wl, inp, temperature, root_from_lm=False, **kw):
     return step, kc, vc, kl
 
 
-def check_full(wl, inp, step, kc, vc, kl, temperature, root_from_lm=False):
+def check_full(wl, inp, step, kc, vc, kl, temperature, root_from_lm=False, tie_break="first"):
     """Whole-step parity with the oracle computing every output."""
     kind = wl.dtype
     tol, delta = TOL[kind], DELTA[kind]
@@ -84,7 +84,7 @@ def check_full(wl, inp, step, kc, vc, kl, temperature, root_from_lm=False):
     zv = oracle.verify_logits(o["X"], o["lm_head"])
     assert rel_err(step.logits, zv) < tol
     near += accept_parity(step, zv, npi(step.tokens), tt, temperature, wl.posterior_threshold,
-                          wl.posterior_alpha, delta, kind)
+                          wl.posterior_alpha, delta, kind, tie_break=tie_break)
     if temperature > 0:
         H_o = np.array([[oracle.node_posterior(zv[b, i], 0, temperature, 0.09, 0.3)["H"] for i in range(tt.T)]
                         for b in range(wl.B)])
@@ -338,3 +338,45 @@ def test_rope_step_matches_oracle(mb, name, near_ties):
             assert torch.equal(kc[b, :, kl0[b] + d], step.k_rot[b, node])
             assert torch.equal(vc[b, :, kl0[b] + d], inp.v_new[b, node])
     near_ties(0)
+
+
+# ----------------------------------------------------------------------------- tie-break variants
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_joint_probability_tie_break_hand_example(mb, dtype):
+    """The hand-built 2 x 3 tree of the oracle's pin, fed through medusa_verify_accept (an
+    identity lm_head, so each node's hidden state carries its logits): the first-in-order
+    rule keeps node (0,0), the joint-probability rule node (1,2) with tokens 0, 2, 5."""
+    tree = mb.Tree(synth.cartesian_choices((2, 3)))
+    T, H, V = 9, 8, 6
+    X = torch.zeros(1, T, H, dtype=torch.float64)
+    X[0, 0, :6] = torch.log(torch.tensor([1, 3, 1, 1, 1, 1.0], dtype=torch.float64))
+    X[0, 1, :6] = torch.log(torch.tensor([1, 1, 1, 2, 1, 1.0], dtype=torch.float64))
+    X[0, 2, :6] = torch.log(torch.tensor([1, 1, 1, 1, 1, 40.0], dtype=torch.float64))
+    X = X.to(dtype).cuda()
+    lm = torch.zeros(V, H, dtype=dtype, device="cuda")
+    lm[torch.arange(V), torch.arange(V)] = 1
+    tokens = torch.tensor([[0, 1, 2, 3, 4, 5, 3, 4, 5]], dtype=torch.int32, device="cuda")
+    dc = mb.MEDUSA_BF16 if dtype == torch.bfloat16 else mb.MEDUSA_F32
+    ws = mb.workspace(mb.medusa_verify_accept_workspace_size(tree, 1, H, V, dc), "cuda")
+    res = {}
+    for rule in ("first", "joint"):
+        out = [torch.full((1,), -1, dtype=torch.int32, device="cuda") for _ in range(4)]
+        acc_tok = torch.full((1, 3), -9, dtype=torch.int32, device="cuda")
+        mb.medusa_verify_accept(tree, X, lm, tokens, 1.0, 0.09, 0.3, out[0], out[1], out[2], acc_tok, out[3], ws,
+                                tie_break=rule)
+        torch.cuda.synchronize()
+        res[rule] = (int(out[0]), int(out[2]), acc_tok[0].tolist())
+    assert res["first"] == (2, 3, [0, 1, 3])
+    assert res["joint"] == (2, 8, [0, 2, 5])
+
+
+@pytest.mark.parametrize("temperature", [0.0, 0.7])
+@pytest.mark.parametrize("wl", [SMALL_BF16, SMALL_BF16_D64], ids=lambda w: w.name)
+def test_joint_tie_break_step(mb, wl, temperature, near_ties):
+    """Whole step with the joint-probability tie-break against the oracle's (random inputs
+    accept many equally deep nodes at temperature 0.7, so the rule decides)."""
+    inp = synth.make_inputs(wl, "cuda")
+    step, kc, vc, kl = run_step(mb, wl, inp, temperature, tie_break="joint")
+    near = near_ties(check_full(wl, inp, step, kc, vc, kl, temperature, tie_break="joint"))
+    assert near <= 3
