@@ -30,6 +30,6 @@ where a function's docstring says "parity unpinned".
 from .medusa import (  # noqa: F401
     bf16_round, medusa_heads, tree_heads, head_topk, base_root,
     TreeTables, tree_tables, tree_tokens,
-    apply_rope, tree_attention, verify_logits, node_posterior, typical_accept, kv_commit,
+    apply_rope, tree_attention, verify_logits, node_posterior, nucleus_next, typical_accept, kv_commit,
     run_step, StepResult,
 )

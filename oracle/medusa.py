@@ -335,6 +335,41 @@ def node_posterior(z_parent: np.ndarray, token: int, temperature: float,
     return dict(p=p, H=H, thr=float(thr), accept=bool(p > thr), margin=float(margin), argmax=top)
 
 
+def nucleus_next(z: np.ndarray, temperature: float, top_p: float, u: float) -> Dict[str, float]:
+    """Next token drawn from the top-p nucleus of softmax(z / temperature), with the
+    draw u in [0, 1) given [CNN "Posterior probability evaluation":
+    evaluate_posterior(..., top_p=top_p, sampling=sampling) names nucleus sampling].
+
+    Reading (the pages name the parameter only): the nucleus is the shortest run
+    of tokens in descending probability, equal probabilities by the lower id,
+    whose mass reaches top_p; the draw picks by inverse CDF over the nucleus
+    renormalised, tokens in ascending id order (the first token whose running
+    mass exceeds u times the nucleus mass).  Temperature 0 is the greedy token.
+    Returns the token, the nucleus size and a margin for near-tie accounting
+    (the smallest gap, relative to the nucleus mass, between u times the mass
+    and a running-mass step, or between top_p and the mass at the nucleus edge).
+    """
+    z = np.asarray(z, np.float64)
+    V = z.size
+    if temperature == 0.0:
+        srt = np.sort(z)
+        return dict(token=int(np.argmax(z)), size=1, margin=float(srt[-1] - srt[-2]) if V > 1 else np.inf)
+    y = (z - z.max()) / temperature
+    q = np.exp(y)
+    q /= q.sum()
+    order = np.lexsort((np.arange(V), -q))
+    cum = np.cumsum(q[order])
+    n = min(V, int(np.searchsorted(cum, top_p, side="left")) + 1)
+    members = np.sort(order[:n])
+    mass = float(q[members].sum())
+    target = u * mass
+    run = np.cumsum(q[members])
+    j = min(n - 1, int(np.searchsorted(run, target, side="right")))
+    edge = [abs(cum[n - 1] - top_p)] + ([abs(cum[n - 2] - top_p)] if n >= 2 else [])
+    margin = min(float(np.min(np.abs(run - target))) / mass, min(edge))
+    return dict(token=int(members[j]), size=n, margin=margin)
+
+
 def typical_accept(z: np.ndarray, tokens: np.ndarray, tt: TreeTables, temperature: float,
                    threshold: float, alpha: float, tie_break: str = "first") -> Dict[str, np.ndarray]:
     """Longest accepted prefix of the candidate tree, per request.

@@ -457,6 +457,35 @@ def test_joint_probability_tie_break_hand_example():
     assert g0["best_node"][0] == f0["best_node"][0]
 
 
+def test_nucleus_hand_example():
+    """q = (0.1, 0.2, 0.7) (logits ln q, temperature 1), top_p = 0.75: by descending
+    probability 0.7 < 0.75, then 0.7 + 0.2 = 0.9 >= 0.75, so the nucleus is tokens {1, 2}
+    with mass 0.9.  In id order the running mass is 0.2, 0.9: u = 0.2 -> target 0.18 ->
+    token 1; u = 0.5 -> target 0.45 -> token 2; u = 0.99 -> token 2."""
+    z = np.log([0.1, 0.2, 0.7])
+    for u, want in ((0.2, 1), (0.5, 2), (0.99, 2)):
+        r = oracle.nucleus_next(z, 1.0, 0.75, u)
+        assert (r["token"], r["size"]) == (want, 2)
+    assert oracle.nucleus_next(z, 1.0, 0.75, 0.2)["margin"] > 0.01
+
+
+def test_nucleus_limits():
+    """top_p -> 0+ keeps only the most probable token (greedy for every draw); top_p = 1
+    keeps every token, and the draw then follows the plain inverse CDF (brute force over a
+    cumulative sum in id order); temperature 0 is the greedy token."""
+    r = _rng(31)
+    z = r.standard_normal(50) * 2
+    top = int(np.argmax(z))
+    for u in (0.0, 0.3, 0.999):
+        assert oracle.nucleus_next(z, 0.7, 1e-9, u)["token"] == top
+    q = np.exp(z / 0.7 - np.max(z / 0.7))
+    q /= q.sum()
+    for u in (0.01, 0.37, 0.8):
+        brute = next(i for i, c in enumerate(np.cumsum(q)) if c > u)
+        assert oracle.nucleus_next(z, 0.7, 1.0, u)["token"] == brute
+    assert oracle.nucleus_next(z, 0.0, 0.9, 0.5)["token"] == top
+
+
 def test_kv_commit_rows_and_overflow():
     tt = oracle.tree_tables(synth.cartesian_choices((2, 3)))
     r = _rng(7)
