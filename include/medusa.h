@@ -315,6 +315,27 @@ int medusa_verify_accept(const medusa_tree* tree, const void* x, const void* lm_
                          void* ws, size_t ws_bytes, medusa_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * medusa_sample_next
+ * The next token drawn from the top-p nucleus of the accepted node's
+ * distribution softmax(z[best_node] / temperature), instead of its greedy
+ * token (cnnetsun "Posterior probability evaluation": evaluate_posterior takes
+ * top_p and a sampling mode; the pages define neither, so this library's
+ * reading is stated here).  The nucleus is the shortest run of tokens in
+ * descending probability (equal logits by the lower id) whose mass reaches
+ * top_p; the draw picks by inverse CDF over the nucleus renormalised, tokens in
+ * ascending id order: the first token whose running mass exceeds
+ * uniform[b] times the nucleus mass.  The random draw is an input, so a step is
+ * reproducible from its inputs; temperature 0 gives the greedy token.
+ *   logits [B,T,V] fp32: medusa_verify_accept's logits output (the call must
+ *   have been given a logits buffer); best_node [B] from the same call;
+ *   uniform [B] fp32 in [0, 1) device; next_token [B] int32 out.
+ *   0 < top_p <= 1.
+ * ---------------------------------------------------------------------- */
+int medusa_sample_next(const medusa_tree* tree, const float* logits, const int32_t* best_node,
+                       const float* uniform, int32_t B, int32_t V, float temperature, float top_p,
+                       int32_t* next_token, medusa_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * medusa_kv_commit
  * The kept branch continues the sequence (Ultralytics "Tree attention and
  * accepting tokens"; wiblog "Inference flow"): the K/V rows of the nodes

@@ -9,7 +9,7 @@ from ._binding import (  # noqa: F401
     medusa_build_tree, medusa_heads_topk, medusa_heads_topk_tree, medusa_heads_topk_tree_workspace_size,
     medusa_heads_topk_workspace_size, kernel_launches, medusa_kv_commit,
     medusa_tree_attention, medusa_tree_attention_workspace_size, medusa_verify_accept,
-    medusa_verify_accept_workspace_size, workspace,
+    medusa_sample_next, medusa_verify_accept_workspace_size, workspace,
 )
 from .step import MedusaStep  # noqa: F401
 

@@ -81,6 +81,7 @@ _sig("medusa_verify_accept_workspace_size", _sz, [_vp, _i32, _i32, _i32, ctypes.
 _sig("medusa_verify_accept", ctypes.c_int,
      [_vp, _vp, _vp, _vp, _i32, _i32, _i32, ctypes.c_int, _f32, _f32, _f32, _i32, _vp, _vp, _vp, _vp, _vp, _vp,
       _vp, _vp, _vp, _vp, _sz, _vp])
+_sig("medusa_sample_next", ctypes.c_int, [_vp, _vp, _vp, _vp, _i32, _i32, _f32, _f32, _vp, _vp])
 _sig("medusa_kv_commit", ctypes.c_int,
      [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, ctypes.c_int, _vp, _vp])
 
@@ -257,3 +258,11 @@ def medusa_kv_commit(tree: Tree, k_new, v_new, k_cache, v_cache, kv_len, best_no
     _check("medusa_kv_commit", lib.medusa_kv_commit(
         tree.handle, _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache), _ptr(kv_len), _ptr(best_node), B,
         Hkv, D, Lmax, dtype_code(k_cache), _ptr(dev_status), _stream(stream)))
+
+
+def medusa_sample_next(tree: Tree, logits, best_node, uniform, temperature: float, top_p: float, next_token,
+                       stream=None) -> None:
+    B, T, V = logits.shape
+    _check("medusa_sample_next", lib.medusa_sample_next(
+        tree.handle, _ptr(logits), _ptr(best_node), _ptr(uniform), B, V, temperature, top_p, _ptr(next_token),
+        _stream(stream)))

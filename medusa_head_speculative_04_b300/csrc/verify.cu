@@ -935,7 +935,210 @@ int dispatch_tc(const VerifyPlan& p, const CUtensorMap& mx, const CUtensorMap& m
   }
 }
 
+// ------------------------------------------------------------------------
+// Nucleus (top-p) draw of the next token from the accepted node's logits, with
+// the uniform draw given: one CTA per request.  The nucleus is the shortest run
+// of tokens in descending probability (equal values by the lower id) whose mass
+// reaches top_p; the draw picks by inverse CDF over the renormalised nucleus,
+// tokens in ascending id order.  The nucleus edge is found by bisection on the
+// ordered bit patterns of the logits (mass(z >= t) is monotone in t), tied
+// tokens at the edge are taken by id, and the draw uses a block scan.
+// ------------------------------------------------------------------------
+constexpr int kSampleThreads = 1024;
+
+__device__ inline uint32_t to_ordered(float f) {
+  const uint32_t u = __float_as_uint(f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ inline float from_ordered(uint32_t o) {
+  return __uint_as_float((o & 0x80000000u) ? (o & 0x7fffffffu) : ~o);
+}
+
+// Block-wide sum (all threads receive it).
+__device__ inline float block_sum(float v, float* red) {
+  v = warp_sum(v);
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  __syncthreads();
+  if (lane == 0) red[w] = v;
+  __syncthreads();
+  float t = lane < static_cast<int>(blockDim.x >> 5) ? red[lane] : 0.f;
+  return warp_sum(t);
+}
+
+// Block-wide exclusive prefix sum of one value per thread (and the total).
+template <typename U>
+__device__ inline U block_excl_scan(U v, U* red, U& total) {
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  U x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const U y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  __syncthreads();
+  if (lane == 31) red[w] = x;
+  __syncthreads();
+  if (w == 0) {
+    U t = lane < static_cast<int>(blockDim.x >> 5) ? red[lane] : U(0);
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const U y = __shfl_up_sync(0xffffffffu, t, o);
+      if (lane >= o) t += y;
+    }
+    red[lane] = t;  // inclusive prefix of warp sums
+  }
+  __syncthreads();
+  total = red[(blockDim.x >> 5) - 1];
+  return (w > 0 ? red[w - 1] : U(0)) + x - v;
+}
+
+__global__ void __launch_bounds__(kSampleThreads) nucleus_next_kernel(const float* __restrict__ logits,
+                                                                      const int32_t* __restrict__ best,
+                                                                      const float* __restrict__ uniform, int T, int V,
+                                                                      float inv_tau, float top_p,
+                                                                      int32_t* __restrict__ next_token) {
+  __shared__ float s_redf[32];
+  __shared__ int s_redi[32];
+  __shared__ float s_m;
+  __shared__ int s_arg;
+  const int b = blockIdx.x;
+  pdl_wait();
+  pdl_trigger();
+  const int node = min(max(best[b], 0), T - 1);
+  const float* z = logits + (static_cast<size_t>(b) * T + node) * V;
+  // maximum (first on ties) and minimum
+  float m = -INFINITY, mn = INFINITY;
+  int arg = 0x7fffffff;
+  for (int v = threadIdx.x; v < V; v += blockDim.x) {
+    const float x = z[v];
+    if (better(x, v, m, arg)) { m = x; arg = v; }
+    mn = fminf(mn, x);
+  }
+  warp_argmax(m, arg);
+  for (int o = 16; o > 0; o >>= 1) mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  __shared__ float s_min[32];
+  if (lane == 0) { s_redf[w] = m; s_redi[w] = arg; s_min[w] = mn; }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float bm = -INFINITY;
+    int ba = 0x7fffffff;
+    for (int i = 0; i < static_cast<int>(blockDim.x >> 5); ++i)
+      if (better(s_redf[i], s_redi[i], bm, ba)) { bm = s_redf[i]; ba = s_redi[i]; }
+    s_m = bm;
+    s_arg = ba;
+  }
+  __syncthreads();
+  const float M = s_m;
+  if (inv_tau == 0.f) {
+    if (threadIdx.x == 0) next_token[b] = s_arg;
+    return;
+  }
+  float zmin = s_min[0];
+  for (int i = 1; i < static_cast<int>(blockDim.x >> 5); ++i) zmin = fminf(zmin, s_min[i]);
+  const float k2 = inv_tau * 1.4426950408889634f;
+  auto q_of = [&](float x) { return ex2_approx((x - M) * k2); };
+  // mass of the tokens whose logit is at least t (unnormalised)
+  auto mass_ge = [&](float t) {
+    float acc = 0.f;
+    for (int v = threadIdx.x; v < V; v += blockDim.x) {
+      const float x = z[v];
+      acc += x >= t ? q_of(x) : 0.f;
+    }
+    return block_sum(acc, s_redf);
+  };
+  const float S = mass_ge(-INFINITY);
+  const float goal = top_p * S;
+  // largest t (a logit value) with mass(z >= t) >= goal: the smallest logit of the nucleus
+  uint32_t lo = to_ordered(zmin), hi = to_ordered(M);
+  if (top_p < 1.f) {
+    while (lo < hi) {
+      const uint32_t mid = lo + (hi - lo + 1) / 2;
+      if (mass_ge(from_ordered(mid)) >= goal) lo = mid; else hi = mid - 1;
+    }
+  }
+  const float tstar = from_ordered(lo);
+  // tokens tied at the edge join by id until the mass is reached
+  float above = 0.f;
+  int ties = 0;
+  for (int v = threadIdx.x; v < V; v += blockDim.x) {
+    const float x = z[v];
+    above += x > tstar ? q_of(x) : 0.f;
+    ties += x == tstar;
+  }
+  above = block_sum(above, s_redf);
+  int n_ties = 0;
+  {
+    int tt = ties;
+    for (int o = 16; o > 0; o >>= 1) tt += __shfl_xor_sync(0xffffffffu, tt, o);
+    __syncthreads();
+    if (lane == 0) s_redi[w] = tt;
+    __syncthreads();
+    for (int i = 0; i < static_cast<int>(blockDim.x >> 5); ++i) n_ties += s_redi[i];
+  }
+  const float qt = q_of(tstar);
+  int take = top_p >= 1.f ? n_ties : static_cast<int>(ceilf((goal - above) / qt));
+  take = min(max(take, 1), n_ties);
+  const float nmass = above + take * qt;
+  const float target = uniform[b] * nmass;
+  // inverse CDF in id order: each thread a contiguous chunk of ids
+  const int C = cdiv(V, blockDim.x);
+  const int v0 = min(V, static_cast<int>(threadIdx.x) * C), v1 = min(V, v0 + C);
+  int my_ties = 0;
+  for (int v = v0; v < v1; ++v) my_ties += z[v] == tstar;
+  __syncthreads();
+  int ties_total = 0;
+  const int tie_before = block_excl_scan<int>(my_ties, s_redi, ties_total);
+  float my_mass = 0.f;
+  {
+    int tr = tie_before;
+    for (int v = v0; v < v1; ++v) {
+      const float x = z[v];
+      const bool in = x > tstar || (x == tstar && tr++ < take);
+      my_mass += in ? q_of(x) : 0.f;
+    }
+  }
+  __syncthreads();
+  float mass_total = 0.f;
+  const float before = block_excl_scan<float>(my_mass, s_redf, mass_total);
+  const bool last_chunk = v1 >= V || (threadIdx.x + 1) * C >= V;
+  if ((before <= target && target < before + my_mass) || (last_chunk && target >= before + my_mass && v0 < V)) {
+    // the draw falls in this chunk (or past the total by rounding: the last member)
+    float run = before;
+    int tr = tie_before, pick = -1, last_member = -1;
+    for (int v = v0; v < v1; ++v) {
+      const float x = z[v];
+      const bool in = x > tstar || (x == tstar && tr++ < take);
+      if (!in) continue;
+      last_member = v;
+      run += q_of(x);
+      if (run > target) { pick = v; break; }
+    }
+    if (pick < 0) pick = last_member;
+    if (pick >= 0) next_token[b] = pick;
+  }
+}
+
 }  // namespace
+
+MEDUSA_API int medusa_sample_next(const medusa_tree* tree, const float* logits, const int32_t* best_node,
+                                  const float* uniform, int32_t B, int32_t V, float temperature, float top_p,
+                                  int32_t* next_token, medusa_stream_t stream) {
+  if (!tree || !logits || !best_node || !uniform || !next_token) return MEDUSA_ERR_INVALID_ARG;
+  if (B < 1 || B > MEDUSA_MAX_BATCH || V < 1 || !(temperature >= 0.f) || !(top_p > 0.f && top_p <= 1.f))
+    return MEDUSA_ERR_INVALID_ARG;
+  const void* ptrs[] = {logits, best_node, uniform, next_token};
+  for (const void* q : ptrs)
+    if (!aligned16(q)) return MEDUSA_ERR_ALIGNMENT;
+  const float inv_tau = temperature > 0.f ? 1.f / temperature : 0.f;
+  if (launch_pdl(nucleus_next_kernel, dim3(B), dim3(kSampleThreads), 0, reinterpret_cast<cudaStream_t>(stream), logits,
+                 best_node, uniform, tree->T, V, inv_tau, top_p, next_token) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return MEDUSA_ERR_CUDA;
+  }
+  MEDUSA_LAUNCH_CHECK();
+  return MEDUSA_OK;
+}
 
 namespace medusa {
 
