@@ -384,11 +384,14 @@ int launch_fc_nb(const HeadsPlan& p, const HeadsWs& w, const T* h, const T* W1, 
 // The tensor-core path (bf16 only): u = h + SiLU(W1_k h + b1_k) with W1 as one
 // [K*H, H] GEMM plus an elementwise launch, then z_k = W2_k u_k as K grouped GEMMs.
 int tc_heads(const HeadsWs&, const float*, const float*, const float*, const float*, int, int, int, int, float*,
-             cudaStream_t) {
+             cudaStream_t, const int32_t* = nullptr, int = 0) {
   return MEDUSA_ERR_UNSUPPORTED;
 }
+// row_keep / keep_T: only the logits of the rows kept are written (the heads over
+// a tree keep each request's accepted row)
 int tc_heads(const HeadsWs& w, const __nv_bfloat16* h, const __nv_bfloat16* W1, const __nv_bfloat16* b1,
-             const __nv_bfloat16* W2, int B, int H, int V, int K, float* z, cudaStream_t st) {
+             const __nv_bfloat16* W2, int B, int H, int V, int K, float* z, cudaStream_t st,
+             const int32_t* row_keep = nullptr, int keep_T = 0) {
   int rc = launch_group_logits_bf16(h, B, 1, W1, H, K * H, w.zfc, st);
   if (rc != MEDUSA_OK) return rc;
   const long n = static_cast<long>(B) * K * H;
@@ -400,7 +403,7 @@ int tc_heads(const HeadsWs& w, const __nv_bfloat16* h, const __nv_bfloat16* W1, 
     return MEDUSA_ERR_CUDA;
   }
   MEDUSA_LAUNCH_CHECK();
-  return launch_group_logits_bf16(w.u, B, K, W2, H, V, z, st);
+  return launch_group_logits_bf16(w.u, B, K, W2, H, V, z, st, row_keep, keep_T);
 }
 
 template <typename T>
@@ -539,7 +542,7 @@ int tree_heads_dispatch(const HeadsPlan& p, const TreeHeadsWs& w, const T* x, co
   const int R = B * Tn;
   if (p.tc) {
     // u and z = W2_k u_k for every row on the tensor cores, then the accepted rows' top-k
-    int rc = tc_heads(w.hw, x, W1, b1, W2, R, H, V, K, w.hw.z, st);
+    int rc = tc_heads(w.hw, x, W1, b1, W2, R, H, V, K, w.hw.z, st, best, Tn);
     if (rc != MEDUSA_OK) return rc;
     for (int b0 = 0; b0 < B; b0 += p.bgroup) {
       rc = launch_vocab_nb<T, true>(p, w.hw, x, W2, static_cast<const T*>(nullptr), B, b0, std::min(p.bgroup, B - b0),

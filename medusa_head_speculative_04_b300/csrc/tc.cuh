@@ -294,8 +294,9 @@ bool make_tmap_bf16_3d(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d
 // n_g row-major bf16 GEMMs on the persistent tcgen05 kernel of the verification
 // pass, fp32 results and no statistics: logits[r][g][v] = sum_i x[r][g][i] *
 // w[g*V + v][i] for r < R, g < n_g, v < V (x is [R][n_g][H], w is [n_g*V][H]).
-// Asynchronous on st; returns a MEDUSA_* status.
+// With row_keep (device, [R / keep_T]) only rows r with r % keep_T ==
+// row_keep[r / keep_T] are written.  Asynchronous on st; returns a MEDUSA_* status.
 int launch_group_logits_bf16(const void* x, int R, int n_g, const void* w, int H, int V, float* logits,
-                             cudaStream_t st);
+                             cudaStream_t st, const int32_t* row_keep = nullptr, int keep_T = 0);
 
 }  // namespace medusa

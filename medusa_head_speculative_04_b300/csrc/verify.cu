@@ -177,6 +177,8 @@ struct EpiArgs {
   float* child_z;
   int32_t* dev_status;
   int n_g;           // GEMMs in the launch (group g: weight rows g*V.., activation group g)
+  const int32_t* row_keep;  // logits only of rows r with r % keep_T == row_keep[r / keep_T] (NULL: all rows)
+  int keep_T;
 };
 
 // ------------------------------------------------------------------------
@@ -295,7 +297,8 @@ __device__ inline void epi_block(const EpiArgs& ea, uint32_t tl, int ch, int nco
   if (!use) return;
   const int c0 = ch * 16;
   const int nv = min(NCH * 16, ncol - c0);
-  if (ea.logits && nv > 0) {
+  if (ea.logits && nv > 0 &&
+      (!ea.row_keep || r % ea.keep_T == min(max(ea.row_keep[r / ea.keep_T], 0), ea.keep_T - 1))) {
     float* dst = ea.logits + (static_cast<size_t>(r) * ea.n_g + g) * ea.V + n0 + c0;
 #pragma unroll
     for (int j = 0; j < NCH * 16; ++j)
@@ -1143,7 +1146,7 @@ MEDUSA_API int medusa_sample_next(const medusa_tree* tree, const float* logits, 
 namespace medusa {
 
 int launch_group_logits_bf16(const void* x, int R, int n_g, const void* w, int H, int V, float* logits,
-                             cudaStream_t st) {
+                             cudaStream_t st, const int32_t* row_keep, int keep_T) {
   if (!x || !w || !logits || R < 1 || n_g < 1 || V < 1 || H < 8 || H % 8 != 0) return MEDUSA_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(w) || !aligned16(logits)) return MEDUSA_ERR_ALIGNMENT;
   const VerifyPlan p = plan_tc(R, n_g, V);
@@ -1152,7 +1155,8 @@ int launch_group_logits_bf16(const void* x, int R, int n_g, const void* w, int H
                             : make_tmap_bf16_3d(&mx, x, H, n_g, R, static_cast<uint64_t>(H) * 2,
                                                 static_cast<uint64_t>(n_g) * H * 2, 1, p.qr);
   if (!okx || !make_tmap_bf16(&mw, w, static_cast<uint64_t>(n_g) * V, H, p.BN)) return MEDUSA_ERR_CUDA;
-  const EpiArgs ea{R, V, 1, 0, nullptr, medusa_tree_dev{}, 0.f, logits, nullptr, nullptr, nullptr, n_g};
+  const EpiArgs ea{R, V, 1, 0, nullptr, medusa_tree_dev{}, 0.f, logits, nullptr, nullptr, nullptr, n_g, row_keep,
+                   keep_T};
   return dispatch_tc(p, mx, mw, H, ea, st);
 }
 
@@ -1191,7 +1195,8 @@ MEDUSA_API int medusa_verify_accept(const medusa_tree* tree, const void* x, cons
   if (!ws || ws_bytes < w.bytes) return MEDUSA_ERR_WORKSPACE;
   auto st = reinterpret_cast<cudaStream_t>(stream);
   const float inv_tau = temperature > 0.f ? 1.f / temperature : 0.f;
-  EpiArgs ea{p.R, V, T, p.n_parts, tree_tokens, tree->dev, inv_tau, logits, w.part, w.child_z, dev_status, 1};
+  EpiArgs ea{p.R, V, T, p.n_parts, tree_tokens, tree->dev, inv_tau, logits, w.part, w.child_z, dev_status, 1,
+             nullptr, 0};
 
   if (dtype == MEDUSA_BF16) {
     CUtensorMap mx, mw;

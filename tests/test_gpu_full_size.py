@@ -12,7 +12,10 @@ import torch
 
 import oracle
 import synth
-from _full import check_attention, check_commit, check_heads, check_tree, check_verify_accept
+import numpy as np
+
+from _full import LazyLogits, check_attention, check_commit, check_heads, check_tree, check_verify_accept
+from _util import TOL, np64, npi, rel_err
 
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 
@@ -39,6 +42,38 @@ CASES = [("llama8b_b1", "plant", 0.0), ("llama8b_b4", "plant", 0.7), ("llama8b_b
          ("ragged7b", "plant", 0.7), ("wide70b", "plant", 0.0), ("wide70b", "random", 0.7)]
 
 
+def tile_rows(wl, T):
+    """The rows of one whole row tile of the verification GEMM (several row tiles: tile m
+    holds rows [4*qr*m, 4*qr*(m+1)), qr rows per TMEM lane quadrant): the middle tile."""
+    R = wl.B * T
+    n_mt = -(-R // 128)
+    qr = -(-R // (4 * n_mt))
+    m = n_mt // 2
+    return [divmod(r, T) for r in range(4 * qr * m, min(R, 4 * qr * (m + 1)))]
+
+
+def check_tile_and_stats(wl, inp, step, tt, temperature, seed=17):
+    """Every logit row of one whole row tile (all four lane quadrants), and node_p / node_H
+    of sampled nodes against the oracle's posterior of their parent's / own row."""
+    lz = LazyLogits(inp.X, inp.lm_head)
+    rows = tile_rows(wl, tt.T)
+    lz.fill(rows)
+    got = np.stack([np64(step.logits[b, i]) for (b, i) in rows])
+    want = np.stack([lz.rows[k] for k in rows])
+    assert rel_err(got, want) < TOL[wl.dtype]
+    rng = np.random.default_rng(seed)
+    picks = [(int(rng.integers(wl.B)), int(rng.integers(1, tt.T))) for _ in range(6)]
+    lz.fill([(b, int(tt.parent[c])) for (b, c) in picks] + picks)
+    tokens = npi(step.tokens)
+    for (b, c) in picks:
+        r = oracle.node_posterior(lz.rows[(b, int(tt.parent[c]))], int(tokens[b, c]), temperature,
+                                  wl.posterior_threshold, wl.posterior_alpha)
+        if temperature > 0:
+            assert abs(float(step.node_p[b, c]) - r["p"]) <= 2e-2 * max(r["p"], 1e-6) + 1e-7, (b, c)
+            Hc = oracle.node_posterior(lz.rows[(b, c)], 0, temperature, 0.09, 0.3)["H"]
+            assert abs(float(step.node_H[b, c]) - Hc) <= 2e-2 * max(Hc, 1.0), (b, c)
+
+
 @pytest.mark.parametrize("name,variant,temperature", CASES)
 def test_full_size_step(mb, name, variant, temperature, near_ties):
     wl = synth.WORKLOADS[name]
@@ -49,6 +84,8 @@ def test_full_size_step(mb, name, variant, temperature, near_ties):
     check_attention(wl, inp, step, tt)
     near += check_verify_accept(wl, inp, step, tt, temperature)
     check_commit(wl, inp, step, kc, vc, kl, tt)
+    if name in ("llama8b_b16", "wide70b"):
+        check_tile_and_stats(wl, inp, step, tt, temperature)
     assert int((step.dev_status & ~1).max()) == 0
     assert near_ties(near) <= max(2, wl.B // 4)
     if variant == "plant":
