@@ -141,8 +141,13 @@ void medusa_tree_destroy(medusa_tree* tree);
  *     not touched (it then holds the previous step's next_root).
  *   For bf16 data u is rounded to bf16 before W2 (the W2 stream is bf16).
  *   Limits: 1 <= B <= MEDUSA_MAX_BATCH, H % 8 == 0, 1 <= topk <= min(V, MEDUSA_MAX_TOPK).
+ *   A row with fewer than topk numbers among its logits (NaN logits) gets id
+ *   -1 and value -inf in the entries left over.
  *   bf16 with B >= 3 and lm_head == NULL runs W1 h and W2_k u_k on the tensor
- *   cores; the workspace then also holds [B,K,V] and [B,K*H] fp32 buffers
+ *   cores; the workspace then also holds the [B,K*H] fp32 first-layer outputs
+ *   and, with topk <= 16, the top-k candidates each vocabulary tile of the W2
+ *   GEMM keeps in its epilogue (a [B,K,tiles,topk] value/id pair, merged per
+ *   row and head by a second launch), else the [B,K,V] fp32 logits
  *   (medusa_heads_topk_workspace_size includes them).
  * ---------------------------------------------------------------------- */
 size_t medusa_heads_topk_workspace_size(int32_t B, int32_t H, int32_t V, int32_t K, int32_t topk,
@@ -170,8 +175,10 @@ int medusa_heads_topk(const void* h, const void* w1, const void* b1, const void*
  *   head_logits [B,K,V] fp32 or NULL: the logits of the accepted rows.
  *   topk_ids, topk_vals [B,K,topk]: as medusa_heads_topk, ready for the next
  *   step's medusa_build_tree together with medusa_verify_accept's next_root.
- *   Limits as medusa_heads_topk.  The workspace holds the [B*T, K, V] logits of
- *   every row (and the [B*T, K*H] first-layer outputs).
+ *   Limits as medusa_heads_topk.  On the tensor cores the workspace holds the
+ *   [B*T, K*H] first-layer outputs and, for the accepted rows only, the tile
+ *   candidates (topk <= 16) or the [B,K,V] logits, as in medusa_heads_topk;
+ *   otherwise the top-k and logits of every row.
  * ---------------------------------------------------------------------- */
 size_t medusa_heads_topk_tree_workspace_size(const medusa_tree* tree, int32_t B, int32_t H, int32_t V,
                                              int32_t K, int32_t topk, medusa_dtype dtype);

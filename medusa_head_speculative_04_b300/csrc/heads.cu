@@ -12,7 +12,8 @@
 // activations).  K2 fuses the top-k: every CTA keeps the top-k of its slice of
 // the vocabulary, and the last CTA of a head (ticket counter) merges them.
 // From kTcMinRows batch rows both products run on the tcgen05 GEMM of the
-// verification pass instead, and K2 only selects from the logits it wrote.
+// verification pass instead; its epilogue keeps the top-k of every vocabulary
+// tile and a small kernel merges the tiles' candidates per (row, head).
 #include <algorithm>
 #include <mutex>
 
@@ -46,6 +47,8 @@ template <int BMAX> struct Pass {
 // CTA's rows lie inside one head and its top-k candidates belong to that head.
 struct HeadsPlan {
   bool tc;      // vocabulary projection on the tensor cores (bf16, >= kTcMinRows rows, root given)
+  bool fused;   // tc, with the top-k in the GEMM epilogue (k <= 16, candidates fit the merge CTA)
+  int ntile;    // fused: vocabulary tiles per head, each contributing k candidates
   int nblk;     // K heads (+1 for the lm_head root block)
   int cph;      // CTAs per block (head)
   int rpc;      // most rows one K2 CTA holds
@@ -77,6 +80,13 @@ int bmax_of(int nb) { return nb == 1 ? 1 : nb == 2 ? 2 : nb <= 4 ? 4 : nb <= 8 ?
 // selects the top-k from them.
 constexpr int kTcMinRows = 3;
 
+// The merge of the tile candidates: [ntile*k] values and ids staged in shared
+// memory, then the block-wide selection's per-warp and final lists.
+size_t merge_smem_bytes(int ntile, int topk) {
+  return (2 * static_cast<size_t>(ntile) * topk + 2 * static_cast<size_t>(kWarps) * topk + 2 * topk) * 4;
+}
+constexpr int kEpiTopkMaxK = 16;  // the GEMM epilogue keeps at most this many per tile
+
 // Returns false when no split fits in shared memory.
 bool plan_heads(int B, int H, int V, int K, int with_root, int esize, int topk, bool allow_tc, HeadsPlan* out) {
   HeadsPlan p{};
@@ -107,36 +117,50 @@ bool plan_heads(int B, int H, int V, int K, int with_root, int esize, int topk, 
   const size_t fc_smem = static_cast<size_t>(p.bgroup) * H * esize;
   const int fc_occ = fc_smem > kSmemTwoPerSm ? 1 : 2;
   p.fc_ctas = static_cast<int>(std::max(1L, std::min(static_cast<long>(sms) * fc_occ, fc_rows)));
+  if (p.tc && topk <= kEpiTopkMaxK) {
+    p.ntile = group_topk_tiles(B, K, V);
+    p.fused = merge_smem_bytes(p.ntile, topk) <= kSmemMax;
+  }
   *out = p;
   return true;
 }
 
 struct HeadsWs {
   void* u;
-  float* z;    // [B, K, V] logits of the tensor-core path when the caller keeps none
+  float* z;    // [out_rows, K, V] logits of the unfused tensor-core path when the caller keeps none
   float* zfc;  // [B, K*H] W1_k h of the tensor-core path
   float* cand_v;
   int* cand_i;
   int* counters;
+  float* tile_v;  // fused: [out_rows, K, ntile, topk] candidates of every vocabulary tile
+  int* tile_i;
   size_t bytes;
 };
 
-HeadsWs carve_heads_ws(void* base, const HeadsPlan& p, int B, int H, int V, int K, int topk, int esize) {
+// B: rows of the head products; out_rows: rows whose top-k is kept (B, or the
+// requests when the heads run over every tree node).
+HeadsWs carve_heads_ws(void* base, const HeadsPlan& p, int B, int H, int V, int K, int topk, int esize,
+                       int out_rows = -1) {
+  if (out_rows < 0) out_rows = B;
   HeadsWs w{};
   size_t o = 0;
   auto take = [&](size_t n) { size_t s = o; o = align_up(o + n, 256); return s; };
   size_t ou = take(static_cast<size_t>(B) * K * H * esize);
-  size_t ncand = static_cast<size_t>(p.nblk) * B * p.cph * topk;
+  size_t ncand = p.fused ? 0 : static_cast<size_t>(p.nblk) * out_rows * p.cph * topk;
   size_t ov = take(ncand * 4), oi = take(ncand * 4), oc = take(static_cast<size_t>(p.nblk) * 4);
-  size_t oz = p.tc ? take(static_cast<size_t>(B) * K * V * 4) : 0;
+  size_t oz = p.tc && !p.fused ? take(static_cast<size_t>(out_rows) * K * V * 4) : 0;
   size_t ozf = p.tc ? take(static_cast<size_t>(B) * K * H * 4) : 0;
+  const size_t ntc = p.fused ? static_cast<size_t>(out_rows) * K * p.ntile * topk : 0;
+  size_t otv = take(ntc * 4), oti = take(ntc * 4);
   char* c = static_cast<char*>(base);
   w.u = c ? c + ou : nullptr;
-  w.z = c && p.tc ? reinterpret_cast<float*>(c + oz) : nullptr;
+  w.z = c && p.tc && !p.fused ? reinterpret_cast<float*>(c + oz) : nullptr;
   w.zfc = c && p.tc ? reinterpret_cast<float*>(c + ozf) : nullptr;
   w.cand_v = c ? reinterpret_cast<float*>(c + ov) : nullptr;
   w.cand_i = c ? reinterpret_cast<int*>(c + oi) : nullptr;
   w.counters = c ? reinterpret_cast<int*>(c + oc) : nullptr;
+  w.tile_v = c && p.fused ? reinterpret_cast<float*>(c + otv) : nullptr;
+  w.tile_i = c && p.fused ? reinterpret_cast<int*>(c + oti) : nullptr;
   w.bytes = o;
   return w;
 }
@@ -218,17 +242,15 @@ __global__ void __launch_bounds__(kThreads) heads_fc_act_kernel(const T* __restr
 // K2: CTA j of block blk holds rows [j*V/cph, (j+1)*V/cph) of that block.
 // Block blk < K is head blk (weights W2_blk, activations u[:, blk]); block K is
 // lm_head on h (root).  FROMZ: the logits were computed by the tensor-core GEMM
-// (zsrc [rows, K, V]) and the CTA only selects from its slice of them; output
-// row b reads source row b, or row b * sel_T + row_sel[b] when row_sel is given
-// (device, read after the dependency wait), and copies it to head_logits when
-// that is given.
+// (zsrc [rows, K, V]) and the CTA only selects from its slice of them, copying
+// it to head_logits when that is given.
 template <typename T, int BMAX, bool FROMZ>
 __global__ void __launch_bounds__(kThreads) heads_vocab_kernel(
     const T* __restrict__ h, const T* __restrict__ u, const T* __restrict__ W2, const T* __restrict__ lm_head,
     int B, int b0, int nb, int H, int V, int K, int topk, int rpc, int cph,
     float* __restrict__ head_logits, int32_t* __restrict__ topk_ids, float* __restrict__ topk_vals,
     int32_t* __restrict__ root_tok, float* __restrict__ cand_v, int* __restrict__ cand_i, int* __restrict__ counters,
-    const float* __restrict__ zsrc, const int32_t* __restrict__ row_sel, int sel_T) {
+    const float* __restrict__ zsrc) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   const int blk = blockIdx.x / cph, cta = blockIdx.x % cph;
   const bool is_root = blk == K;
@@ -258,9 +280,7 @@ __global__ void __launch_bounds__(kThreads) heads_vocab_kernel(
   if (FROMZ) {
     for (int e = threadIdx.x; e < nb * n; e += blockDim.x) {
       const int b = e / n, lr = e % n;
-      const size_t src = row_sel ? static_cast<size_t>(b0 + b) * sel_T + min(max(row_sel[b0 + b], 0), sel_T - 1)
-                                 : static_cast<size_t>(b0 + b);
-      const float z = zsrc[(src * K + blk) * V + v0 + lr];
+      const float z = zsrc[((static_cast<size_t>(b0) + b) * K + blk) * V + v0 + lr];
       zs[static_cast<size_t>(b) * rpc + lr] = z;
       if (head_logits) head_logits[(static_cast<size_t>(b0 + b) * K + blk) * V + v0 + lr] = z;
     }
@@ -345,14 +365,14 @@ int launch_fc(const HeadsPlan& p, const HeadsWs& w, const T* h, const T* W1, con
 template <typename T, int BMAX, bool FROMZ>
 int launch_vocab(const HeadsPlan& p, const HeadsWs& w, const T* h, const T* W2, const T* lm, int B, int b0, int nb,
                  int H, int V, int K, int topk, float* head_logits, int32_t* topk_ids, float* topk_vals,
-                 int32_t* root_tok, const float* zsrc, const int32_t* row_sel, int sel_T, cudaStream_t st) {
+                 int32_t* root_tok, const float* zsrc, cudaStream_t st) {
   const size_t smem = vocab_smem_bytes(nb, BMAX, H, sizeof(T), p.rpc, p.cph, topk);
   auto vk = heads_vocab_kernel<T, BMAX, FROMZ>;
   if (!ensure_dyn_smem(vk, smem))
     return MEDUSA_ERR_CUDA;
   if (launch_pdl(vk, dim3(p.nblk * p.cph), dim3(kThreads), smem, st, h, static_cast<const T*>(w.u), W2, lm, B, b0, nb,
                  H, V, K, topk, p.rpc, p.cph, head_logits, topk_ids, topk_vals, root_tok, w.cand_v, w.cand_i,
-                 w.counters, zsrc, row_sel, sel_T) != cudaSuccess) {
+                 w.counters, zsrc) != cudaSuccess) {
     (void)cudaGetLastError();
     return MEDUSA_ERR_CUDA;
   }
@@ -363,12 +383,12 @@ int launch_vocab(const HeadsPlan& p, const HeadsWs& w, const T* h, const T* W2, 
 template <typename T, bool FROMZ>
 int launch_vocab_nb(const HeadsPlan& p, const HeadsWs& w, const T* h, const T* W2, const T* lm, int B, int b0,
                     int nb, int H, int V, int K, int topk, float* hl, int32_t* ids, float* vals, int32_t* root,
-                    const float* zsrc, cudaStream_t st, const int32_t* row_sel = nullptr, int sel_T = 0) {
-  if (nb == 1) return launch_vocab<T, 1, FROMZ>(p, w, h, W2, lm, B, b0, nb, H, V, K, topk, hl, ids, vals, root, zsrc, row_sel, sel_T, st);
-  if (nb == 2) return launch_vocab<T, 2, FROMZ>(p, w, h, W2, lm, B, b0, nb, H, V, K, topk, hl, ids, vals, root, zsrc, row_sel, sel_T, st);
-  if (nb <= 4) return launch_vocab<T, 4, FROMZ>(p, w, h, W2, lm, B, b0, nb, H, V, K, topk, hl, ids, vals, root, zsrc, row_sel, sel_T, st);
-  if (nb <= 8) return launch_vocab<T, 8, FROMZ>(p, w, h, W2, lm, B, b0, nb, H, V, K, topk, hl, ids, vals, root, zsrc, row_sel, sel_T, st);
-  return launch_vocab<T, 16, FROMZ>(p, w, h, W2, lm, B, b0, nb, H, V, K, topk, hl, ids, vals, root, zsrc, row_sel, sel_T, st);
+                    const float* zsrc, cudaStream_t st) {
+  if (nb == 1) return launch_vocab<T, 1, FROMZ>(p, w, h, W2, lm, B, b0, nb, H, V, K, topk, hl, ids, vals, root, zsrc, st);
+  if (nb == 2) return launch_vocab<T, 2, FROMZ>(p, w, h, W2, lm, B, b0, nb, H, V, K, topk, hl, ids, vals, root, zsrc, st);
+  if (nb <= 4) return launch_vocab<T, 4, FROMZ>(p, w, h, W2, lm, B, b0, nb, H, V, K, topk, hl, ids, vals, root, zsrc, st);
+  if (nb <= 8) return launch_vocab<T, 8, FROMZ>(p, w, h, W2, lm, B, b0, nb, H, V, K, topk, hl, ids, vals, root, zsrc, st);
+  return launch_vocab<T, 16, FROMZ>(p, w, h, W2, lm, B, b0, nb, H, V, K, topk, hl, ids, vals, root, zsrc, st);
 }
 
 template <typename T>
@@ -381,17 +401,62 @@ int launch_fc_nb(const HeadsPlan& p, const HeadsWs& w, const T* h, const T* W1, 
   return launch_fc<T, 16>(p, w, h, W1, b1, b0, nb, H, K, st);
 }
 
+// Merge of the fused path: CTA (b, head) takes the top-k of the ntile*topk
+// candidates its vocabulary tiles left (unfilled ones are NaN and never taken).
+__global__ void __launch_bounds__(kThreads) topk_merge_kernel(const float* __restrict__ tile_v,
+                                                              const int* __restrict__ tile_i, int K, int ntile,
+                                                              int topk, int32_t* __restrict__ topk_ids,
+                                                              float* __restrict__ topk_vals) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  const int n = ntile * topk;
+  float* mv = reinterpret_cast<float*>(smem_raw);
+  int* mi = reinterpret_cast<int*>(mv + n);
+  float* sv = reinterpret_cast<float*>(mi + n);  // [kWarps * topk]
+  int* si = reinterpret_cast<int*>(sv + kWarps * topk);
+  float* fv = reinterpret_cast<float*>(si + kWarps * topk);
+  int* fi = reinterpret_cast<int*>(fv + topk);
+  pdl_wait();
+  pdl_trigger();
+  const size_t base = static_cast<size_t>(blockIdx.x) * n;  // blockIdx.x = b * K + head
+  for (int e = threadIdx.x; e < n; e += blockDim.x) {
+    mv[e] = tile_v[base + e];
+    mi[e] = tile_i[base + e];
+  }
+  __syncthreads();
+  block_topk(mv, mi, 0, n, topk, fv, fi, sv, si);
+  for (int t = threadIdx.x; t < topk; t += blockDim.x) {
+    topk_ids[static_cast<size_t>(blockIdx.x) * topk + t] = fi[t];
+    topk_vals[static_cast<size_t>(blockIdx.x) * topk + t] = fv[t];
+  }
+}
+
+int launch_topk_merge(const HeadsPlan& p, const HeadsWs& w, int rows, int K, int topk, int32_t* ids, float* vals,
+                      cudaStream_t st) {
+  const size_t smem = merge_smem_bytes(p.ntile, topk);
+  if (!ensure_dyn_smem(topk_merge_kernel, smem))
+    return MEDUSA_ERR_CUDA;
+  if (launch_pdl(topk_merge_kernel, dim3(rows * K), dim3(kThreads), smem, st, static_cast<const float*>(w.tile_v),
+                 static_cast<const int*>(w.tile_i), K, p.ntile, topk, ids, vals) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return MEDUSA_ERR_CUDA;
+  }
+  MEDUSA_LAUNCH_CHECK();
+  return MEDUSA_OK;
+}
+
 // The tensor-core path (bf16 only): u = h + SiLU(W1_k h + b1_k) with W1 as one
-// [K*H, H] GEMM plus an elementwise launch, then z_k = W2_k u_k as K grouped GEMMs.
-int tc_heads(const HeadsWs&, const float*, const float*, const float*, const float*, int, int, int, int, float*,
-             cudaStream_t, const int32_t* = nullptr, int = 0) {
+// [K*H, H] GEMM plus an elementwise launch, then z_k = W2_k u_k as K grouped
+// GEMMs: fused, with the tiles' top-k candidates into the workspace (and the
+// logits into z when z is given); else the logits into z.
+int tc_heads(const HeadsPlan&, const HeadsWs&, const float*, const float*, const float*, const float*, int, int, int,
+             int, int, float*, cudaStream_t, const int32_t* = nullptr, int = 0) {
   return MEDUSA_ERR_UNSUPPORTED;
 }
-// row_keep / keep_T: only the logits of the rows kept are written (the heads over
+// row_keep / keep_T: only the rows kept are written, compactly (the heads over
 // a tree keep each request's accepted row)
-int tc_heads(const HeadsWs& w, const __nv_bfloat16* h, const __nv_bfloat16* W1, const __nv_bfloat16* b1,
-             const __nv_bfloat16* W2, int B, int H, int V, int K, float* z, cudaStream_t st,
-             const int32_t* row_keep = nullptr, int keep_T = 0) {
+int tc_heads(const HeadsPlan& p, const HeadsWs& w, const __nv_bfloat16* h, const __nv_bfloat16* W1,
+             const __nv_bfloat16* b1, const __nv_bfloat16* W2, int B, int H, int V, int K, int topk, float* z,
+             cudaStream_t st, const int32_t* row_keep = nullptr, int keep_T = 0) {
   int rc = launch_group_logits_bf16(h, B, 1, W1, H, K * H, w.zfc, st);
   if (rc != MEDUSA_OK) return rc;
   const long n = static_cast<long>(B) * K * H;
@@ -403,6 +468,8 @@ int tc_heads(const HeadsWs& w, const __nv_bfloat16* h, const __nv_bfloat16* W1, 
     return MEDUSA_ERR_CUDA;
   }
   MEDUSA_LAUNCH_CHECK();
+  if (p.fused)
+    return launch_group_topk_bf16(w.u, B, K, W2, H, V, topk, w.tile_v, w.tile_i, z, st, row_keep, keep_T);
   return launch_group_logits_bf16(w.u, B, K, W2, H, V, z, st, row_keep, keep_T);
 }
 
@@ -412,8 +479,12 @@ int heads_dispatch(const HeadsPlan& p, const HeadsWs& w, const T* h, const T* W1
                    int32_t* root, cudaStream_t st) {
   if (p.tc) {
     // u and z = W2_k u_k on the tensor cores, then the top-k of z
+    if (p.fused) {
+      const int rc = tc_heads(p, w, h, W1, b1, W2, B, H, V, K, topk, hl, st);
+      return rc != MEDUSA_OK ? rc : launch_topk_merge(p, w, B, K, topk, ids, vals, st);
+    }
     float* z = hl ? hl : w.z;
-    int rc = tc_heads(w, h, W1, b1, W2, B, H, V, K, z, st);
+    int rc = tc_heads(p, w, h, W1, b1, W2, B, H, V, K, topk, z, st);
     if (rc != MEDUSA_OK) return rc;
     for (int b0 = 0; b0 < B; b0 += p.bgroup) {
       rc = launch_vocab_nb<T, true>(p, w, h, W2, lm, B, b0, std::min(p.bgroup, B - b0), H, V, K, topk, nullptr, ids,
@@ -517,9 +588,10 @@ struct TreeHeadsWs {
   size_t bytes;
 };
 
-TreeHeadsWs carve_tree_heads_ws(void* base, const HeadsPlan& p, int R, int H, int V, int K, int topk, int es) {
+TreeHeadsWs carve_tree_heads_ws(void* base, const HeadsPlan& p, int B, int R, int H, int V, int K, int topk,
+                                int es) {
   TreeHeadsWs w{};
-  w.hw = carve_heads_ws(base, p, R, H, V, K, topk, es);
+  w.hw = carve_heads_ws(base, p, R, H, V, K, topk, es, p.tc ? B : R);
   size_t o = w.hw.bytes;
   auto take = [&](size_t n) { size_t s = o; o = align_up(o + n, 256); return s; };
   const size_t nk = static_cast<size_t>(R) * K * topk;
@@ -541,12 +613,17 @@ int tree_heads_dispatch(const HeadsPlan& p, const TreeHeadsWs& w, const T* x, co
                         float* vals, cudaStream_t st) {
   const int R = B * Tn;
   if (p.tc) {
-    // u and z = W2_k u_k for every row on the tensor cores, then the accepted rows' top-k
-    int rc = tc_heads(w.hw, x, W1, b1, W2, R, H, V, K, w.hw.z, st, best, Tn);
+    // u and z = W2_k u_k for every row on the tensor cores; the accepted rows'
+    // candidates (or logits) are kept, one row per request
+    if (p.fused) {
+      const int rc = tc_heads(p, w.hw, x, W1, b1, W2, R, H, V, K, topk, hl, st, best, Tn);
+      return rc != MEDUSA_OK ? rc : launch_topk_merge(p, w.hw, B, K, topk, ids, vals, st);
+    }
+    int rc = tc_heads(p, w.hw, x, W1, b1, W2, R, H, V, K, topk, w.hw.z, st, best, Tn);
     if (rc != MEDUSA_OK) return rc;
     for (int b0 = 0; b0 < B; b0 += p.bgroup) {
       rc = launch_vocab_nb<T, true>(p, w.hw, x, W2, static_cast<const T*>(nullptr), B, b0, std::min(p.bgroup, B - b0),
-                                    H, V, K, topk, hl, ids, vals, nullptr, w.hw.z, st, best, Tn);
+                                    H, V, K, topk, hl, ids, vals, nullptr, w.hw.z, st);
       if (rc != MEDUSA_OK) return rc;
     }
     return MEDUSA_OK;
@@ -573,7 +650,7 @@ MEDUSA_API size_t medusa_heads_topk_tree_workspace_size(const medusa_tree* tree,
   const int R = B * tree->T;
   HeadsPlan p;
   if (!plan_heads(R, H, V, K, 0, es, topk, true, &p)) return 0;
-  return carve_tree_heads_ws(nullptr, p, R, H, V, K, topk, es).bytes;
+  return carve_tree_heads_ws(nullptr, p, B, R, H, V, K, topk, es).bytes;
 }
 
 MEDUSA_API int medusa_heads_topk_tree(const medusa_tree* tree, const void* x, const void* w1, const void* b1,
@@ -594,7 +671,7 @@ MEDUSA_API int medusa_heads_topk_tree(const medusa_tree* tree, const void* x, co
   const int Tn = tree->T, R = B * Tn;
   HeadsPlan p;
   if (!plan_heads(R, H, V, K, 0, es, topk, true, &p)) return MEDUSA_ERR_UNSUPPORTED;
-  TreeHeadsWs w = carve_tree_heads_ws(ws, p, R, H, V, K, topk, es);
+  TreeHeadsWs w = carve_tree_heads_ws(ws, p, B, R, H, V, K, topk, es);
   if (!ws || ws_bytes < w.bytes) return MEDUSA_ERR_WORKSPACE;
   auto st = reinterpret_cast<cudaStream_t>(stream);
   if (dtype == MEDUSA_BF16)

@@ -95,7 +95,7 @@ struct VerifyPlan {
 // is one 224-column tile per CTA.  With several row tiles the GEMM is
 // compute-bound and takes the widest MMA.
 // tcgen05 GEMM plan for R rows, n_g groups and V columns per group.
-VerifyPlan plan_tc(int R, int n_g, int V) {
+VerifyPlan plan_tc(int R, int n_g, int V, bool topk = false) {
   VerifyPlan p{};
   p.R = R;
   const int sms = device_sm_count();
@@ -103,7 +103,8 @@ VerifyPlan plan_tc(int R, int n_g, int V) {
   p.qr = cdiv(R, 4 * p.n_mt);
   if (p.n_mt == 1) {
     long best = -1;
-    for (int bn = 16; bn <= 256; bn += 16) {
+    // the top-k epilogue is built for tile widths 128..256 in steps of 32
+    for (int bn = topk ? 128 : 16; bn <= 256; bn += topk ? 32 : 16) {
       const long per_cta = cdiv(n_g * cdiv(V, bn), sms);
       const long cost = 8 * per_cta * (bn + 8 * p.qr) + bn;
       if (best < 0 || cost <= best) {
@@ -177,9 +178,14 @@ struct EpiArgs {
   float* child_z;
   int32_t* dev_status;
   int n_g;           // GEMMs in the launch (group g: weight rows g*V.., activation group g)
-  const int32_t* row_keep;  // logits only of rows r with r % keep_T == row_keep[r / keep_T] (NULL: all rows)
-  int keep_T;
+  const int32_t* row_keep;  // only rows r with r % keep_T == row_keep[r / keep_T] (NULL: all rows), written
+  int keep_T;               // at row r / keep_T of the logits and candidates
+  int topk_k;        // top-k epilogue: candidates [rows][n_g][n_nt][topk_k] of each (row, group, vocabulary tile)
+  float* cand_v;
+  int* cand_i;
 };
+
+constexpr int kEpiTopkMax = 16;  // most candidates the top-k epilogue keeps per (row, tile)
 
 // ------------------------------------------------------------------------
 // K5, bf16: persistent tcgen05 GEMM with the statistics epilogue.
@@ -205,6 +211,7 @@ constexpr int kWarpW = kEpiWarps, kWarpMma = kEpiWarps + 1, kWarpX = kEpiWarps +
 constexpr int kTcThreads = (kEpiWarps + 3) * 32;
 constexpr int kColGroups = kEpiWarps / 4;
 constexpr size_t kXchgBytes = 2 * (kColGroups - 1) * BM * 5 * 4;  // per-row statistics of groups 1.., 2 buffers
+constexpr size_t kTopkBufBytes = kEpiWarps * 64 * 4;  // top-k epilogue: one 64-column row buffer per warp
 
 struct TcShape {
   int BN;       // vocabulary columns per tile
@@ -215,6 +222,7 @@ struct TcShape {
   int n_tiles;  // n_g * n_nt * n_mt; tile t is row tile t % n_mt, then vocabulary tile, then group
   int sw;       // lm_head ring stages
   int sx;       // X ring stages (<= kMaxStagesX)
+  int topk;     // top-k epilogue (its exchange buffer follows the statistics one)
 };
 
 constexpr float kLog2e = 1.4426950408889634f;
@@ -299,7 +307,8 @@ __device__ inline void epi_block(const EpiArgs& ea, uint32_t tl, int ch, int nco
   const int nv = min(NCH * 16, ncol - c0);
   if (ea.logits && nv > 0 &&
       (!ea.row_keep || r % ea.keep_T == min(max(ea.row_keep[r / ea.keep_T], 0), ea.keep_T - 1))) {
-    float* dst = ea.logits + (static_cast<size_t>(r) * ea.n_g + g) * ea.V + n0 + c0;
+    const int ro = ea.row_keep ? r / ea.keep_T : r;  // kept rows are written compactly
+    float* dst = ea.logits + (static_cast<size_t>(ro) * ea.n_g + g) * ea.V + n0 + c0;
 #pragma unroll
     for (int j = 0; j < NCH * 16; ++j)
       if (j < nv) dst[j] = v[j];
@@ -320,7 +329,83 @@ __device__ inline void epi_block(const EpiArgs& ea, uint32_t tl, int ch, int nco
 
 __device__ inline bool failed(const volatile int* f) { return *f != 0; }
 
+// Top-k epilogue of one accumulator tile for the rows in `rows` (bits = lanes
+// of this warp's quadrant).  Per row: its columns go through `buf` (one lane
+// stores 64 columns, all lanes read two), so the row's top-k is a list spread
+// over lanes 0..k-1 (value descending, equal values by the lower column) and a
+// column enters only if it beats the k-th entry: a ballot finds such columns,
+// each insertion counts the entries ahead of it and shifts the rest down one
+// lane.  NaN never enters.  The row's k entries go to the candidate buffer
+// (unfilled ones as NaN / -1), and its logits to ea.logits when that is given.
 template <int BN>
+__device__ __forceinline__ void topk_tile(const EpiArgs& ea, uint32_t tl, int ncol, int n0, int r_lane, int g, int n_t,
+                                       uint32_t rows, float* buf) {
+  constexpr int NCH = BN / 16;  // a multiple of 2: loads of 4 chunks, then possibly one of 2
+  const int lane = threadIdx.x & 31, k = ea.topk_k;
+  for (; rows; rows &= rows - 1) {
+    const int rr = __ffs(rows) - 1;
+    const int r = __shfl_sync(0xffffffffu, r_lane, rr);
+    const int ro = ea.row_keep ? r / ea.keep_T : r;
+    float* zrow = ea.logits ? ea.logits + (static_cast<size_t>(ro) * ea.n_g + g) * ea.V + n0 : nullptr;
+    float lv = -INFINITY, tv = -INFINITY;  // lane j < k: entry j; tv/ti: entry k-1
+    int li = 0x7fffffff, ti = 0x7fffffff;
+#pragma unroll 1
+    for (int ch = 0; ch < NCH; ch += 4) {
+      float v[64];
+      int nc = 4;
+      if (NCH - ch >= 4) {
+        tc::tmem_ld16n<4>(tl + ch * 16, v);
+      } else {
+        tc::tmem_ld16n<2>(tl + ch * 16, *reinterpret_cast<float(*)[32]>(v));
+        nc = 2;
+      }
+      if (lane == rr) {
+#pragma unroll
+        for (int q = 0; q < 16; ++q)
+          if (q < nc * 4) *reinterpret_cast<float4*>(buf + 4 * q) = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+      }
+      __syncwarp();
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int c = ch * 16 + h * 32 + lane;
+        const bool in = h * 32 < nc * 16 && c < ncol;
+        const float x = in ? buf[h * 32 + lane] : __int_as_float(0x7fc00000);
+        const int id = n0 + c;
+        if (zrow && in) zrow[c] = x;
+        uint32_t cand = __ballot_sync(0xffffffffu, better(x, id, tv, ti));
+        while (cand) {
+          const int src = __ffs(cand) - 1;
+          const float xv = __shfl_sync(0xffffffffu, x, src);
+          const int xi = __shfl_sync(0xffffffffu, id, src);
+          // x beats entry k-1, so fewer than k entries are ahead of it
+          const int pos = __popc(__ballot_sync(0xffffffffu, lane < k && better(lv, li, xv, xi)));
+          const float uv = __shfl_up_sync(0xffffffffu, lv, 1);
+          const int ui = __shfl_up_sync(0xffffffffu, li, 1);
+          if (lane == pos) {
+            lv = xv;
+            li = xi;
+          } else if (lane > pos && lane < k) {
+            lv = uv;
+            li = ui;
+          }
+          tv = __shfl_sync(0xffffffffu, lv, k - 1);
+          ti = __shfl_sync(0xffffffffu, li, k - 1);
+          cand &= cand - 1;
+          cand &= __ballot_sync(0xffffffffu, better(x, id, tv, ti));
+        }
+      }
+      __syncwarp();
+    }
+    if (lane < k) {
+      const size_t o = ((static_cast<size_t>(ro) * ea.n_g + g) * ea.n_nt + n_t) * k + lane;
+      const bool filled = li != 0x7fffffff;
+      ea.cand_v[o] = filled ? lv : __int_as_float(0x7fc00000);
+      ea.cand_i[o] = filled ? li : -1;
+    }
+  }
+}
+
+template <int BN, bool TOPK>
 __global__ void __launch_bounds__(kTcThreads, 1) verify_tc_kernel(const __grid_constant__ CUtensorMap tma_x,
                                                                  const __grid_constant__ CUtensorMap tma_w, int H,
                                                                  TcShape sh, EpiArgs ea) {
@@ -340,6 +425,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) verify_tc_kernel(const __grid_c
   uint64_t* acc_empty = acc_full + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 2);
   float* xh = reinterpret_cast<float*>(tmem_slot + 4);  // [2][kColGroups-1][5][BM] statistics of groups 1..
+  float* tbuf = xh + kXchgBytes / 4;  // top-k epilogue: [kEpiWarps][64] one row's columns
   __shared__ int s_fail;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -497,6 +583,18 @@ __global__ void __launch_bounds__(kTcThreads, 1) verify_tc_kernel(const __grid_c
       }
       ok = ok && __all_sync(0xffffffffu, !failed(&s_fail) && tc::mbar_wait(acc_full + a, (jl >> 1) & 1));
       tc::fence_after_sync();
+      if constexpr (TOPK) {
+        // the two warps of a lane quadrant split its kept rows by parity; each
+        // takes its rows' whole tile, one row at a time, across its 32 lanes
+        const bool keep = valid_row && (!ea.row_keep || r % ea.keep_T == min(max(ea.row_keep[r / ea.keep_T], 0),
+                                                                              ea.keep_T - 1));
+        const uint32_t mine = __ballot_sync(0xffffffffu, keep) & (grp ? 0xaaaaaaaau : 0x55555555u);
+        if (ok && mine) topk_tile<BN>(ea, tl, ncol, n0, r, g, n_t, mine, tbuf + warp * 64);
+        tc::fence_before_sync();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(acc_empty + a);
+        continue;
+      }
       float m = -INFINITY, s = 0.f, w2 = 0.f;
       int arg = n0 + ch0 * 16;
       bool nan_seen = false;
@@ -889,8 +987,9 @@ __global__ void __launch_bounds__(kMergeRows * 32) merge_accept_kernel(AcceptArg
 constexpr size_t kTcSmemMax = 227 * 1024 - 1024;  // the kernel's static shared memory takes 1 KB
 constexpr size_t kTcFixedBytes = 1024 + (2 * kMaxStagesW + 2 * kMaxStagesX + 4) * 8 + 16 + kXchgBytes;
 
-TcShape tc_shape(const VerifyPlan& p) {
+TcShape tc_shape(const VerifyPlan& p, bool topk = false) {
   TcShape sh{};
+  sh.topk = topk ? 1 : 0;
   sh.BN = p.BN;
   sh.qr = p.qr;
   sh.n_mt = p.n_mt;
@@ -901,21 +1000,23 @@ TcShape tc_shape(const VerifyPlan& p) {
   // three X stages (L2 latency); the rest of shared memory goes to the weight
   // ring, which also carries the prefetch made before the dependency wait
   sh.sx = 3;
-  sh.sw = static_cast<int>(std::min<size_t>(kMaxStagesW, (kTcSmemMax - kTcFixedBytes - sh.sx * kXStageBytes) / wb));
+  const size_t fixed = kTcFixedBytes + (topk ? kTopkBufBytes : 0);
+  sh.sw = static_cast<int>(std::min<size_t>(kMaxStagesW, (kTcSmemMax - fixed - sh.sx * kXStageBytes) / wb));
   return sh;
 }
 
 size_t tc_smem_bytes(const TcShape& sh) {
-  return kTcFixedBytes + static_cast<size_t>(sh.sx) * kXStageBytes + static_cast<size_t>(sh.sw) * sh.BN * BK * 2;
+  return kTcFixedBytes + (sh.topk ? kTopkBufBytes : 0) + static_cast<size_t>(sh.sx) * kXStageBytes +
+         static_cast<size_t>(sh.sw) * sh.BN * BK * 2;
 }
 
-template <int BN>
+template <int BN, bool TOPK>
 int launch_tc(const VerifyPlan& p, const CUtensorMap& mx, const CUtensorMap& mw, int H, const EpiArgs& ea,
               cudaStream_t st) {
-  const TcShape sh = tc_shape(p);
+  const TcShape sh = tc_shape(p, TOPK);
   if (sh.sw < 2) return MEDUSA_ERR_UNSUPPORTED;
   const size_t smem = tc_smem_bytes(sh);
-  auto k = verify_tc_kernel<BN>;
+  auto k = verify_tc_kernel<BN, TOPK>;
   if (!ensure_dyn_smem(k, smem))
     return MEDUSA_ERR_CUDA;
   if (launch_pdl(k, dim3(p.grid), dim3(kTcThreads), smem, st, mx, mw, H, sh, ea) != cudaSuccess) {
@@ -928,8 +1029,17 @@ int launch_tc(const VerifyPlan& p, const CUtensorMap& mx, const CUtensorMap& mw,
 
 int dispatch_tc(const VerifyPlan& p, const CUtensorMap& mx, const CUtensorMap& mw, int H, const EpiArgs& ea,
                 cudaStream_t st) {
+  if (ea.topk_k > 0) {
+    if (ea.topk_k > kEpiTopkMax || !ea.cand_v || !ea.cand_i) return MEDUSA_ERR_INVALID_ARG;
+    switch (p.BN) {
+#define MEDUSA_BN(n) case n: return launch_tc<n, true>(p, mx, mw, H, ea, st);
+      MEDUSA_BN(128) MEDUSA_BN(160) MEDUSA_BN(192) MEDUSA_BN(224) MEDUSA_BN(256)
+#undef MEDUSA_BN
+      default: return MEDUSA_ERR_UNSUPPORTED;
+    }
+  }
   switch (p.BN) {
-#define MEDUSA_BN(n) case n: return launch_tc<n>(p, mx, mw, H, ea, st);
+#define MEDUSA_BN(n) case n: return launch_tc<n, false>(p, mx, mw, H, ea, st);
     MEDUSA_BN(16) MEDUSA_BN(32) MEDUSA_BN(48) MEDUSA_BN(64) MEDUSA_BN(80) MEDUSA_BN(96) MEDUSA_BN(112)
     MEDUSA_BN(128) MEDUSA_BN(144) MEDUSA_BN(160) MEDUSA_BN(176) MEDUSA_BN(192) MEDUSA_BN(208) MEDUSA_BN(224)
     MEDUSA_BN(240) MEDUSA_BN(256)
@@ -1147,7 +1257,8 @@ namespace medusa {
 
 int launch_group_logits_bf16(const void* x, int R, int n_g, const void* w, int H, int V, float* logits,
                              cudaStream_t st, const int32_t* row_keep, int keep_T) {
-  if (!x || !w || !logits || R < 1 || n_g < 1 || V < 1 || H < 8 || H % 8 != 0) return MEDUSA_ERR_INVALID_ARG;
+  if (!x || !w || !logits || R < 1 || n_g < 1 || V < 1 || H < 8 || H % 8 != 0 || (row_keep && keep_T < 1))
+    return MEDUSA_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(w) || !aligned16(logits)) return MEDUSA_ERR_ALIGNMENT;
   const VerifyPlan p = plan_tc(R, n_g, V);
   CUtensorMap mx, mw;
@@ -1157,6 +1268,25 @@ int launch_group_logits_bf16(const void* x, int R, int n_g, const void* w, int H
   if (!okx || !make_tmap_bf16(&mw, w, static_cast<uint64_t>(n_g) * V, H, p.BN)) return MEDUSA_ERR_CUDA;
   const EpiArgs ea{R, V, 1, 0, nullptr, medusa_tree_dev{}, 0.f, logits, nullptr, nullptr, nullptr, n_g, row_keep,
                    keep_T};
+  return dispatch_tc(p, mx, mw, H, ea, st);
+}
+
+int group_topk_tiles(int R, int n_g, int V) { return plan_tc(R, n_g, V, true).n_nt; }
+
+int launch_group_topk_bf16(const void* x, int R, int n_g, const void* w, int H, int V, int k, float* cand_v,
+                           int* cand_i, float* logits, cudaStream_t st, const int32_t* row_keep, int keep_T) {
+  if (!x || !w || !cand_v || !cand_i || R < 1 || n_g < 1 || V < 1 || H < 8 || H % 8 != 0 || k < 1 ||
+      k > kEpiTopkMax || (row_keep && keep_T < 1))
+    return MEDUSA_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(w) || (logits && !aligned16(logits))) return MEDUSA_ERR_ALIGNMENT;
+  const VerifyPlan p = plan_tc(R, n_g, V, true);
+  CUtensorMap mx, mw;
+  const bool okx = n_g == 1 ? make_tmap_bf16(&mx, x, R, H, p.qr)
+                            : make_tmap_bf16_3d(&mx, x, H, n_g, R, static_cast<uint64_t>(H) * 2,
+                                                static_cast<uint64_t>(n_g) * H * 2, 1, p.qr);
+  if (!okx || !make_tmap_bf16(&mw, w, static_cast<uint64_t>(n_g) * V, H, p.BN)) return MEDUSA_ERR_CUDA;
+  const EpiArgs ea{R,   V,        1,      p.n_nt, nullptr, medusa_tree_dev{}, 0.f, logits, nullptr, nullptr,
+                   nullptr, n_g, row_keep, keep_T, k,     cand_v,  cand_i};
   return dispatch_tc(p, mx, mw, H, ea, st);
 }
 

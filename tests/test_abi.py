@@ -102,13 +102,19 @@ def test_binding_has_no_cpu_path():
 
 def test_heads_workspace_holds_the_tensor_core_buffers(lib):
     """bf16 with three or more batch rows and the root given takes the tensor-core heads
-    path, whose workspace also holds the [B,K,V] logits and the [B,K*H] W1 h buffers; the
-    lm_head-root variant and fp32 stay on the CUDA-core path without them."""
+    path, whose workspace also holds the [B,K*H] W1 h buffer and either the top-k
+    candidates of every vocabulary tile (k <= 16: tiles 128 to 256 columns wide) or the
+    [B,K,V] logits (k > 16); the lm_head-root variant and fp32 stay on the CUDA-core path
+    without them."""
     f = lib.lib.medusa_heads_topk_workspace_size
     B, H, V, K, topk = 3, 4096, 32000, 5, 10
-    extra = B * K * V * 4 + B * K * H * 4
+    fc = B * K * H * 4
+    cand_lo, cand_hi = B * K * (V // 256) * topk * 8, B * K * -(-V // 128) * topk * 8
     tc = f(B, H, V, K, topk, 0, 1)
-    assert tc >= extra
-    assert 0 < f(B, H, V, K, topk, 1, 1) < extra
-    assert 0 < f(B, H, V, K, topk, 0, 0) < extra
-    assert 0 < f(2, H, V, K, topk, 0, 1) < extra
+    assert fc + cand_lo <= tc < fc + cand_hi + B * K * H * 2 + 64 * 1024
+    assert tc < B * K * V * 4          # the logits stay out of the workspace
+    assert f(B, H, V, K, 17, 0, 1) >= B * K * V * 4 + fc
+    base = fc + cand_lo
+    assert 0 < f(B, H, V, K, topk, 1, 1) < base
+    assert 0 < f(B, H, V, K, topk, 0, 0) < base
+    assert 0 < f(2, H, V, K, topk, 0, 1) < base
