@@ -431,13 +431,16 @@ __global__ void __launch_bounds__(kTcThreads, 1) verify_tc_kernel(const __grid_c
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nk = cdiv(H, BK);
   const int qr = sh.qr;
-  // In the memory-bound GEMM (one row tile) CTAs start their K loops at
-  // different blocks, spreading the concurrent requests over more DRAM pages;
-  // the compute-bound one keeps the CTAs that share a weight tile in step, so
-  // the tile is still in L2 for all of them
-  // (one GEMM only: the tiles of grouped GEMMs keep one summation order, so
-  // equal groups give bit-identical results)
-  const int rot = sh.n_mt == 1 && sh.n_g == 1 ? static_cast<int>((static_cast<long>(blockIdx.x) * nk) / gridDim.x) : 0;
+  // In the memory-bound GEMM (one row tile) the K loop of vocabulary tile n_t
+  // starts at block n_t * nk / n_nt, so the CTAs streaming at the same time
+  // spread their requests over more DRAM pages; the rotation depends on the
+  // column tile only, so every group of a grouped GEMM sums a column in the
+  // same order (equal groups give bit-identical results).  The compute-bound
+  // GEMM keeps the CTAs that share a weight tile in step, so the tile is still
+  // in L2 for all of them.
+  auto rot_of = [&](int t) {
+    return sh.n_mt == 1 ? static_cast<int>((static_cast<long>((t / sh.n_mt) % sh.n_nt) * nk) / sh.n_nt) : 0;
+  };
 
   if (threadIdx.x == 0) {
     s_fail = 0;
@@ -472,6 +475,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) verify_tc_kernel(const __grid_c
       for (int t = blockIdx.x; t < sh.n_tiles && run; t += gridDim.x) {
         const int rest = t / sh.n_mt;
         const int wrow = (rest / sh.n_nt) * ea.V + (rest % sh.n_nt) * BN;  // group g's rows start at g*V
+        const int rot = rot_of(t);
         for (int k = 0; k < nk; ++k, ++i) {
           const int s = i % sh.sw;
           if (failed(&s_fail) || !tc::mbar_wait(wempty + s, ((i / sh.sw) & 1) ^ 1)) { s_fail = 1; run = false; break; }
@@ -489,6 +493,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) verify_tc_kernel(const __grid_c
       for (int t = blockIdx.x; t < sh.n_tiles && run; t += gridDim.x) {
         const int row0 = (t % sh.n_mt) * 4 * qr;
         const int g = t / sh.n_mt / sh.n_nt;
+        const int rot = rot_of(t);
         for (int k = 0; k < nk; ++k, ++i) {
           const int s = i % sh.sx;
           if (failed(&s_fail) || !tc::mbar_wait(xempty + s, ((i / sh.sx) & 1) ^ 1)) { s_fail = 1; run = false; break; }
