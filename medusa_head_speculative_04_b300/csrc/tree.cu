@@ -218,10 +218,8 @@ __global__ void build_tree_kernel(medusa_tree_dev tr, const int32_t* __restrict_
     s_rank[i] = static_cast<int16_t>(tr.rank[i]);
   }
   __syncthreads();
-  // the next kernel may start its set-up now: it waits for this grid to complete
-  // before it reads anything this step produced
-  pdl_trigger();
   pdl_wait();
+  pdl_trigger();
   const int32_t L = kv_len[b];
   const int32_t root = root_tok[b];
   bool bad = root < 0;
