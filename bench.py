@@ -318,41 +318,39 @@ def run_ours(args, ws, rank, local):
     for a in step.accept_len.cpu().tolist():
         accept_hist[str(a)] = accept_hist.get(str(a), 0) + 1
 
-    # the steady-state loop: the next step's candidates come from the heads over
-    # every tree node of this step (expand, attend, verify + accept, commit, heads
-    # over the tree), timed as its own CUDA graph of the same step count
-    steady = None
-    if wl.dtype == "bf16":
-        def steady_step():
-            kl.copy_(kv_len0)
-            step.build(kl)
-            step.attention(inp.q, inp.k_new, inp.v_new, kc, vc, kl)
-            step.verify(inp.X, inp.lm_head, tau, wl.posterior_threshold, wl.posterior_alpha)
-            step.commit(inp.k_new, inp.v_new, kc, vc, kl)
-            step.heads_from_tree(inp.X, inp.W1, inp.b1, inp.W2)
-        with torch.cuda.stream(s):
-            steady_step()                       # workspace of the tree heads, kernel attributes
-        torch.cuda.synchronize()
-        gT = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(gT, stream=s):
-            for _ in range(S):
-                steady_step()
-        with torch.cuda.stream(s):
-            for _ in range(max(1, warm // S)):
-                gT.replay()
-        torch.cuda.synchronize()
-        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        with torch.cuda.stream(s):
-            t0.record()
-            for _ in range(reps):
-                gT.replay()
-            t1.record()
-        torch.cuda.synchronize()
-        ms_s = t0.elapsed_time(t1) / max(1, reps * S)
-        steady = {"value": round(wl.B / (ms_s / 1e3), 2), "unit": UNIT, "ms_per_step": round(ms_s, 5),
-                  "note": "steady-state loop: tree expansion from the previous step's accepted row, attention, "
-                          "verification + acceptance, commit, then the heads over every tree node "
-                          "(medusa_heads_topk_tree) for the next step; same workload and step count"}
+    # the steady-state loop: the next step's candidates come from the heads on this
+    # step's accepted tree rows (expand, attend, verify + accept, commit, heads on
+    # the tree rows), timed as its own CUDA graph of the same step count
+    def steady_step():
+        kl.copy_(kv_len0)
+        step.build(kl)
+        step.attention(inp.q, inp.k_new, inp.v_new, kc, vc, kl)
+        step.verify(inp.X, inp.lm_head, tau, wl.posterior_threshold, wl.posterior_alpha)
+        step.commit(inp.k_new, inp.v_new, kc, vc, kl)
+        step.heads_from_tree(inp.X, inp.W1, inp.b1, inp.W2)
+    with torch.cuda.stream(s):
+        steady_step()                       # workspace of the tree heads, kernel attributes
+    torch.cuda.synchronize()
+    gT = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gT, stream=s):
+        for _ in range(S):
+            steady_step()
+    with torch.cuda.stream(s):
+        for _ in range(max(1, warm // S)):
+            gT.replay()
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(s):
+        t0.record()
+        for _ in range(reps):
+            gT.replay()
+        t1.record()
+    torch.cuda.synchronize()
+    ms_s = t0.elapsed_time(t1) / max(1, reps * S)
+    steady = {"value": round(wl.B / (ms_s / 1e3), 2), "unit": UNIT, "ms_per_step": round(ms_s, 5),
+              "note": "steady-state loop: tree expansion from the previous step's accepted row, attention, "
+                      "verification + acceptance, commit, then the heads on each request's accepted tree row "
+                      "(medusa_heads_topk_tree) for the next step; same workload and step count"}
 
     # end-to-end through the public API: every step copies its inputs in from
     # pinned host memory and its results out.  The inputs of step i+1 upload on a

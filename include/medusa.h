@@ -160,14 +160,16 @@ int medusa_heads_topk(const void* h, const void* w1, const void* b1, const void*
 
 /* ------------------------------------------------------------------------
  * medusa_heads_topk_tree
- * The Medusa heads over the hidden state of every tree node, of which each
- * request keeps the top-k of its accepted node: the candidates of the next
- * step come out of the verification pass with no separate pass over the
- * accepted token (wiblog "Inference flow in an online chat service"; the
- * accepted branch continues the sequence, Ultralytics "Tree attention and
- * accepting tokens").  For node row x[b,i]: u_k = x + SiLU(W1_k x + b1_k),
- * z_k = W2_k u_k, computed for all B*T rows (bf16 with B*T >= 3: both head
- * products as tcgen05 GEMMs); request b keeps the top-k of row best_node[b].
+ * The Medusa heads on the tree nodes' hidden states, of which each request
+ * keeps the top-k of its accepted node: the candidates of the next step come
+ * out of the verification pass with no separate pass over the accepted token
+ * (wiblog "Inference flow in an online chat service"; the accepted branch
+ * continues the sequence, Ultralytics "Tree attention and accepting
+ * tokens").  For node row x[b,i]: u_k = x + SiLU(W1_k x + b1_k), z_k = W2_k u_k;
+ * request b keeps the top-k of row best_node[b].  Acceptance is known when
+ * this runs, so the accepted rows are gathered first and the heads run on
+ * those B rows (bf16 with B >= 3: both head products as tcgen05 GEMMs), which
+ * gives the same outputs as running them on every node.
  *   x [B,T,H] (the tree nodes' hidden states, as given to
  *   medusa_verify_accept); w1, b1, w2 as in medusa_heads_topk;
  *   best_node [B] int32 device (medusa_verify_accept's output; values outside
@@ -175,10 +177,8 @@ int medusa_heads_topk(const void* h, const void* w1, const void* b1, const void*
  *   head_logits [B,K,V] fp32 or NULL: the logits of the accepted rows.
  *   topk_ids, topk_vals [B,K,topk]: as medusa_heads_topk, ready for the next
  *   step's medusa_build_tree together with medusa_verify_accept's next_root.
- *   Limits as medusa_heads_topk.  On the tensor cores the workspace holds the
- *   [B*T, K*H] first-layer outputs and, for the accepted rows only, the tile
- *   candidates (topk <= 16) or the [B,K,V] logits, as in medusa_heads_topk;
- *   otherwise the top-k and logits of every row.
+ *   Limits as medusa_heads_topk.  The workspace holds the gathered [B,H] rows
+ *   and medusa_heads_topk's workspace for B rows without lm_head.
  * ---------------------------------------------------------------------- */
 size_t medusa_heads_topk_tree_workspace_size(const medusa_tree* tree, int32_t B, int32_t H, int32_t V,
                                              int32_t K, int32_t topk, medusa_dtype dtype);

@@ -127,30 +127,26 @@ bool plan_heads(int B, int H, int V, int K, int with_root, int esize, int topk, 
 
 struct HeadsWs {
   void* u;
-  float* z;    // [out_rows, K, V] logits of the unfused tensor-core path when the caller keeps none
+  float* z;    // [B, K, V] logits of the unfused tensor-core path when the caller keeps none
   float* zfc;  // [B, K*H] W1_k h of the tensor-core path
   float* cand_v;
   int* cand_i;
   int* counters;
-  float* tile_v;  // fused: [out_rows, K, ntile, topk] candidates of every vocabulary tile
+  float* tile_v;  // fused: [B, K, ntile, topk] candidates of every vocabulary tile
   int* tile_i;
   size_t bytes;
 };
 
-// B: rows of the head products; out_rows: rows whose top-k is kept (B, or the
-// requests when the heads run over every tree node).
-HeadsWs carve_heads_ws(void* base, const HeadsPlan& p, int B, int H, int V, int K, int topk, int esize,
-                       int out_rows = -1) {
-  if (out_rows < 0) out_rows = B;
+HeadsWs carve_heads_ws(void* base, const HeadsPlan& p, int B, int H, int V, int K, int topk, int esize) {
   HeadsWs w{};
   size_t o = 0;
   auto take = [&](size_t n) { size_t s = o; o = align_up(o + n, 256); return s; };
   size_t ou = take(static_cast<size_t>(B) * K * H * esize);
-  size_t ncand = p.fused ? 0 : static_cast<size_t>(p.nblk) * out_rows * p.cph * topk;
+  size_t ncand = p.fused ? 0 : static_cast<size_t>(p.nblk) * B * p.cph * topk;
   size_t ov = take(ncand * 4), oi = take(ncand * 4), oc = take(static_cast<size_t>(p.nblk) * 4);
-  size_t oz = p.tc && !p.fused ? take(static_cast<size_t>(out_rows) * K * V * 4) : 0;
+  size_t oz = p.tc && !p.fused ? take(static_cast<size_t>(B) * K * V * 4) : 0;
   size_t ozf = p.tc ? take(static_cast<size_t>(B) * K * H * 4) : 0;
-  const size_t ntc = p.fused ? static_cast<size_t>(out_rows) * K * p.ntile * topk : 0;
+  const size_t ntc = p.fused ? static_cast<size_t>(B) * K * p.ntile * topk : 0;
   size_t otv = take(ntc * 4), oti = take(ntc * 4);
   char* c = static_cast<char*>(base);
   w.u = c ? c + ou : nullptr;
@@ -449,14 +445,12 @@ int launch_topk_merge(const HeadsPlan& p, const HeadsWs& w, int rows, int K, int
 // GEMMs: fused, with the tiles' top-k candidates into the workspace (and the
 // logits into z when z is given); else the logits into z.
 int tc_heads(const HeadsPlan&, const HeadsWs&, const float*, const float*, const float*, const float*, int, int, int,
-             int, int, float*, cudaStream_t, const int32_t* = nullptr, int = 0) {
+             int, int, float*, cudaStream_t) {
   return MEDUSA_ERR_UNSUPPORTED;
 }
-// row_keep / keep_T: only the rows kept are written, compactly (the heads over
-// a tree keep each request's accepted row)
 int tc_heads(const HeadsPlan& p, const HeadsWs& w, const __nv_bfloat16* h, const __nv_bfloat16* W1,
              const __nv_bfloat16* b1, const __nv_bfloat16* W2, int B, int H, int V, int K, int topk, float* z,
-             cudaStream_t st, const int32_t* row_keep = nullptr, int keep_T = 0) {
+             cudaStream_t st) {
   int rc = launch_group_logits_bf16(h, B, 1, W1, H, K * H, w.zfc, st);
   if (rc != MEDUSA_OK) return rc;
   const long n = static_cast<long>(B) * K * H;
@@ -469,8 +463,8 @@ int tc_heads(const HeadsPlan& p, const HeadsWs& w, const __nv_bfloat16* h, const
   }
   MEDUSA_LAUNCH_CHECK();
   if (p.fused)
-    return launch_group_topk_bf16(w.u, B, K, W2, H, V, topk, w.tile_v, w.tile_i, z, st, row_keep, keep_T);
-  return launch_group_logits_bf16(w.u, B, K, W2, H, V, z, st, row_keep, keep_T);
+    return launch_group_topk_bf16(w.u, B, K, W2, H, V, topk, w.tile_v, w.tile_i, z, st);
+  return launch_group_logits_bf16(w.u, B, K, W2, H, V, z, st);
 }
 
 template <typename T>
@@ -545,65 +539,46 @@ MEDUSA_API int medusa_heads_topk(const void* h, const void* w1, const void* b1, 
 }
 
 // ---------------------------------------------------------------------------
-// medusa_heads_topk_tree: the heads over the hidden state of every tree node
-// (rows b*T + i of x), of which each request keeps the top-k of its accepted
-// node for the next step.  wiblog.cn "Medusa multi-head speculative decoding",
-// section "Inference flow in an online chat service": the verification pass
-// that scores the candidates also yields what the next round's candidates come
-// from, with no extra forward pass; Ultralytics glossary "Medusa Heads",
-// section "Tree attention and accepting tokens": the accepted branch continues
-// the sequence.  The rows' count B*T makes both head products dense GEMMs
-// (bf16: the tcgen05 path), and the top-k runs only on the accepted rows.
+// medusa_heads_topk_tree: the next step's candidates from the verification
+// pass's hidden states.  wiblog.cn "Medusa multi-head speculative decoding",
+// section "Inference flow in an online chat service": the pass that scores the
+// candidates also yields what the next round's candidates come from, with no
+// extra forward pass; Ultralytics glossary "Medusa Heads", section "Tree
+// attention and accepting tokens": the accepted branch continues the sequence.
+// Only the accepted node's heads are kept, and acceptance is known when this
+// runs, so each request's accepted row x[b, best_node[b]] is gathered first and
+// the heads run on those B rows (the same outputs as running them on every
+// node and keeping the accepted one, for B rows of work instead of B*T).
 // ---------------------------------------------------------------------------
 namespace {
 
-// CUDA-core path: request b's top-k (and logits) copied from row b*T + best[b].
-__global__ void __launch_bounds__(256) gather_topk_kernel(const int32_t* __restrict__ ids_all,
-                                                          const float* __restrict__ vals_all,
-                                                          const float* __restrict__ logits_all,
-                                                          const int32_t* __restrict__ best, int T, int K, int topk,
-                                                          int V, int32_t* __restrict__ ids, float* __restrict__ vals,
-                                                          float* __restrict__ logits) {
+// xg[b] = x[b, clamp(best[b])] (16-byte chunks).
+template <typename T>
+__global__ void __launch_bounds__(256) gather_rows_kernel(const T* __restrict__ x, const int32_t* __restrict__ best,
+                                                          int Tn, int H, T* __restrict__ xg) {
   const int b = blockIdx.x;
   pdl_wait();
   pdl_trigger();
-  const int node = min(max(best[b], 0), T - 1);
-  const size_t src = static_cast<size_t>(b) * T + node;
-  const int nk = K * topk;
-  for (int e = threadIdx.x; e < nk; e += blockDim.x) {
-    ids[static_cast<size_t>(b) * nk + e] = ids_all[src * nk + e];
-    vals[static_cast<size_t>(b) * nk + e] = vals_all[src * nk + e];
-  }
-  if (logits) {
-    const size_t nv = static_cast<size_t>(K) * V;
-    for (size_t e = threadIdx.x; e < nv; e += blockDim.x) logits[b * nv + e] = logits_all[src * nv + e];
-  }
+  const int node = min(max(best[b], 0), Tn - 1);
+  constexpr int E = Elem<T>::kPer16B;
+  const uint4* src = reinterpret_cast<const uint4*>(x + (static_cast<size_t>(b) * Tn + node) * H);
+  uint4* dst = reinterpret_cast<uint4*>(xg + static_cast<size_t>(b) * H);
+  for (int c = threadIdx.x; c < H / E; c += blockDim.x) dst[c] = src[c];
 }
 
 struct TreeHeadsWs {
-  HeadsWs hw;
-  int32_t* ids_all;    // CUDA-core path: [B*T, K, topk]
-  float* vals_all;
-  float* logits_all;   // CUDA-core path: [B*T, K, V]
+  void* xg;      // [B, H] the accepted rows
+  HeadsWs hw;    // the heads on those rows
   size_t bytes;
 };
 
-TreeHeadsWs carve_tree_heads_ws(void* base, const HeadsPlan& p, int B, int R, int H, int V, int K, int topk,
-                                int es) {
+TreeHeadsWs carve_tree_heads_ws(void* base, const HeadsPlan& p, int B, int H, int V, int K, int topk, int es) {
   TreeHeadsWs w{};
-  w.hw = carve_heads_ws(base, p, R, H, V, K, topk, es, p.tc ? B : R);
-  size_t o = w.hw.bytes;
-  auto take = [&](size_t n) { size_t s = o; o = align_up(o + n, 256); return s; };
-  const size_t nk = static_cast<size_t>(R) * K * topk;
-  const size_t oi = p.tc ? 0 : take(nk * 4), ov = p.tc ? 0 : take(nk * 4);
-  const size_t ol = p.tc ? 0 : take(static_cast<size_t>(R) * K * V * 4);
+  const size_t gx = align_up(static_cast<size_t>(B) * H * es, 256);
   char* c = static_cast<char*>(base);
-  if (c && !p.tc) {
-    w.ids_all = reinterpret_cast<int32_t*>(c + oi);
-    w.vals_all = reinterpret_cast<float*>(c + ov);
-    w.logits_all = reinterpret_cast<float*>(c + ol);
-  }
-  w.bytes = o;
+  w.xg = c;
+  w.hw = carve_heads_ws(c ? c + gx : nullptr, p, B, H, V, K, topk, es);
+  w.bytes = gx + w.hw.bytes;
   return w;
 }
 
@@ -611,34 +586,14 @@ template <typename T>
 int tree_heads_dispatch(const HeadsPlan& p, const TreeHeadsWs& w, const T* x, const T* W1, const T* b1, const T* W2,
                         const int32_t* best, int B, int Tn, int H, int V, int K, int topk, float* hl, int32_t* ids,
                         float* vals, cudaStream_t st) {
-  const int R = B * Tn;
-  if (p.tc) {
-    // u and z = W2_k u_k for every row on the tensor cores; the accepted rows'
-    // candidates (or logits) are kept, one row per request
-    if (p.fused) {
-      const int rc = tc_heads(p, w.hw, x, W1, b1, W2, R, H, V, K, topk, hl, st, best, Tn);
-      return rc != MEDUSA_OK ? rc : launch_topk_merge(p, w.hw, B, K, topk, ids, vals, st);
-    }
-    int rc = tc_heads(p, w.hw, x, W1, b1, W2, R, H, V, K, topk, w.hw.z, st, best, Tn);
-    if (rc != MEDUSA_OK) return rc;
-    for (int b0 = 0; b0 < B; b0 += p.bgroup) {
-      rc = launch_vocab_nb<T, true>(p, w.hw, x, W2, static_cast<const T*>(nullptr), B, b0, std::min(p.bgroup, B - b0),
-                                    H, V, K, topk, hl, ids, vals, nullptr, w.hw.z, st);
-      if (rc != MEDUSA_OK) return rc;
-    }
-    return MEDUSA_OK;
-  }
-  int rc = heads_dispatch(p, w.hw, x, W1, b1, W2, static_cast<const T*>(nullptr), R, H, V, K, topk, w.logits_all,
-                          w.ids_all, w.vals_all, nullptr, st);
-  if (rc != MEDUSA_OK) return rc;
-  if (launch_pdl(gather_topk_kernel, dim3(B), dim3(256), 0, st, static_cast<const int32_t*>(w.ids_all),
-                 static_cast<const float*>(w.vals_all), static_cast<const float*>(w.logits_all), best, Tn, K, topk, V,
-                 ids, vals, hl) != cudaSuccess) {
+  if (launch_pdl(gather_rows_kernel<T>, dim3(B), dim3(256), 0, st, x, best, Tn, H, static_cast<T*>(w.xg)) !=
+      cudaSuccess) {
     (void)cudaGetLastError();
     return MEDUSA_ERR_CUDA;
   }
   MEDUSA_LAUNCH_CHECK();
-  return MEDUSA_OK;
+  return heads_dispatch(p, w.hw, static_cast<const T*>(w.xg), W1, b1, W2, static_cast<const T*>(nullptr), B, H, V,
+                        K, topk, hl, ids, vals, static_cast<int32_t*>(nullptr), st);
 }
 
 }  // namespace
@@ -647,10 +602,9 @@ MEDUSA_API size_t medusa_heads_topk_tree_workspace_size(const medusa_tree* tree,
                                                         int32_t K, int32_t topk, medusa_dtype dtype) {
   if (!tree || B < 1 || H < 8 || V < 1 || K < 1 || topk < 1) return 0;
   const int es = dtype == MEDUSA_BF16 ? 2 : 4;
-  const int R = B * tree->T;
   HeadsPlan p;
-  if (!plan_heads(R, H, V, K, 0, es, topk, true, &p)) return 0;
-  return carve_tree_heads_ws(nullptr, p, B, R, H, V, K, topk, es).bytes;
+  if (!plan_heads(B, H, V, K, 0, es, topk, true, &p)) return 0;
+  return carve_tree_heads_ws(nullptr, p, B, H, V, K, topk, es).bytes;
 }
 
 MEDUSA_API int medusa_heads_topk_tree(const medusa_tree* tree, const void* x, const void* w1, const void* b1,
@@ -668,10 +622,10 @@ MEDUSA_API int medusa_heads_topk_tree(const medusa_tree* tree, const void* x, co
     if (!aligned16(q)) return MEDUSA_ERR_ALIGNMENT;
   if ((head_logits && !aligned16(head_logits)) || (ws && !aligned16(ws))) return MEDUSA_ERR_ALIGNMENT;
   const int es = dtype == MEDUSA_BF16 ? 2 : 4;
-  const int Tn = tree->T, R = B * Tn;
+  const int Tn = tree->T;
   HeadsPlan p;
-  if (!plan_heads(R, H, V, K, 0, es, topk, true, &p)) return MEDUSA_ERR_UNSUPPORTED;
-  TreeHeadsWs w = carve_tree_heads_ws(ws, p, B, R, H, V, K, topk, es);
+  if (!plan_heads(B, H, V, K, 0, es, topk, true, &p)) return MEDUSA_ERR_UNSUPPORTED;
+  TreeHeadsWs w = carve_tree_heads_ws(ws, p, B, H, V, K, topk, es);
   if (!ws || ws_bytes < w.bytes) return MEDUSA_ERR_WORKSPACE;
   auto st = reinterpret_cast<cudaStream_t>(stream);
   if (dtype == MEDUSA_BF16)

@@ -294,21 +294,18 @@ bool make_tmap_bf16_3d(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d
 // n_g row-major bf16 GEMMs on the persistent tcgen05 kernel of the verification
 // pass, fp32 results and no statistics: logits[r][g][v] = sum_i x[r][g][i] *
 // w[g*V + v][i] for r < R, g < n_g, v < V (x is [R][n_g][H], w is [n_g*V][H]).
-// With row_keep (device, [R / keep_T]) only rows r with r % keep_T ==
-// row_keep[r / keep_T] are written, at row r / keep_T of logits ([R / keep_T]
-// rows).  Asynchronous on st; returns a MEDUSA_* status.
+// Asynchronous on st; returns a MEDUSA_* status.
 int launch_group_logits_bf16(const void* x, int R, int n_g, const void* w, int H, int V, float* logits,
-                             cudaStream_t st, const int32_t* row_keep = nullptr, int keep_T = 0);
+                             cudaStream_t st);
 
 // The same grouped GEMM with a top-k epilogue instead of the logits: for every
 // (row, group, vocabulary tile of group_topk_tiles(R, n_g, V) tiles) the k
 // largest logits of the tile (equal values by the lower column, NaN never
 // taken) go to cand_v / cand_i [R][n_g][tiles][k]; entries of a tile with fewer
 // than k numbers are (NaN, -1).  k <= 16.  The logits are written too when
-// `logits` is given.  row_keep as above (candidates of row r at row r / keep_T).
+// `logits` is given.
 int group_topk_tiles(int R, int n_g, int V);
 int launch_group_topk_bf16(const void* x, int R, int n_g, const void* w, int H, int V, int k, float* cand_v,
-                           int* cand_i, float* logits, cudaStream_t st, const int32_t* row_keep = nullptr,
-                           int keep_T = 0);
+                           int* cand_i, float* logits, cudaStream_t st);
 
 }  // namespace medusa

@@ -178,8 +178,6 @@ struct EpiArgs {
   float* child_z;
   int32_t* dev_status;
   int n_g;           // GEMMs in the launch (group g: weight rows g*V.., activation group g)
-  const int32_t* row_keep;  // only rows r with r % keep_T == row_keep[r / keep_T] (NULL: all rows), written
-  int keep_T;               // at row r / keep_T of the logits and candidates
   int topk_k;        // top-k epilogue: candidates [rows][n_g][n_nt][topk_k] of each (row, group, vocabulary tile)
   float* cand_v;
   int* cand_i;
@@ -305,10 +303,8 @@ __device__ inline void epi_block(const EpiArgs& ea, uint32_t tl, int ch, int nco
   if (!use) return;
   const int c0 = ch * 16;
   const int nv = min(NCH * 16, ncol - c0);
-  if (ea.logits && nv > 0 &&
-      (!ea.row_keep || r % ea.keep_T == min(max(ea.row_keep[r / ea.keep_T], 0), ea.keep_T - 1))) {
-    const int ro = ea.row_keep ? r / ea.keep_T : r;  // kept rows are written compactly
-    float* dst = ea.logits + (static_cast<size_t>(ro) * ea.n_g + g) * ea.V + n0 + c0;
+  if (ea.logits && nv > 0) {
+    float* dst = ea.logits + (static_cast<size_t>(r) * ea.n_g + g) * ea.V + n0 + c0;
 #pragma unroll
     for (int j = 0; j < NCH * 16; ++j)
       if (j < nv) dst[j] = v[j];
@@ -345,8 +341,7 @@ __device__ __forceinline__ void topk_tile(const EpiArgs& ea, uint32_t tl, int nc
   for (; rows; rows &= rows - 1) {
     const int rr = __ffs(rows) - 1;
     const int r = __shfl_sync(0xffffffffu, r_lane, rr);
-    const int ro = ea.row_keep ? r / ea.keep_T : r;
-    float* zrow = ea.logits ? ea.logits + (static_cast<size_t>(ro) * ea.n_g + g) * ea.V + n0 : nullptr;
+    float* zrow = ea.logits ? ea.logits + (static_cast<size_t>(r) * ea.n_g + g) * ea.V + n0 : nullptr;
     float lv = -INFINITY, tv = -INFINITY;  // lane j < k: entry j; tv/ti: entry k-1
     int li = 0x7fffffff, ti = 0x7fffffff;
 #pragma unroll 1
@@ -397,7 +392,7 @@ __device__ __forceinline__ void topk_tile(const EpiArgs& ea, uint32_t tl, int nc
       __syncwarp();
     }
     if (lane < k) {
-      const size_t o = ((static_cast<size_t>(ro) * ea.n_g + g) * ea.n_nt + n_t) * k + lane;
+      const size_t o = ((static_cast<size_t>(r) * ea.n_g + g) * ea.n_nt + n_t) * k + lane;
       const bool filled = li != 0x7fffffff;
       ea.cand_v[o] = filled ? lv : __int_as_float(0x7fc00000);
       ea.cand_i[o] = filled ? li : -1;
@@ -589,11 +584,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) verify_tc_kernel(const __grid_c
       ok = ok && __all_sync(0xffffffffu, !failed(&s_fail) && tc::mbar_wait(acc_full + a, (jl >> 1) & 1));
       tc::fence_after_sync();
       if constexpr (TOPK) {
-        // the two warps of a lane quadrant split its kept rows by parity; each
-        // takes its rows' whole tile, one row at a time, across its 32 lanes
-        const bool keep = valid_row && (!ea.row_keep || r % ea.keep_T == min(max(ea.row_keep[r / ea.keep_T], 0),
-                                                                              ea.keep_T - 1));
-        const uint32_t mine = __ballot_sync(0xffffffffu, keep) & (grp ? 0xaaaaaaaau : 0x55555555u);
+        // the two warps of a lane quadrant split its rows by parity; each takes
+        // its rows' whole tile, one row at a time, across its 32 lanes
+        const uint32_t mine = __ballot_sync(0xffffffffu, valid_row) & (grp ? 0xaaaaaaaau : 0x55555555u);
         if (ok && mine) topk_tile<BN>(ea, tl, ncol, n0, r, g, n_t, mine, tbuf + warp * 64);
         tc::fence_before_sync();
         __syncwarp();
@@ -1261,8 +1254,8 @@ MEDUSA_API int medusa_sample_next(const medusa_tree* tree, const float* logits, 
 namespace medusa {
 
 int launch_group_logits_bf16(const void* x, int R, int n_g, const void* w, int H, int V, float* logits,
-                             cudaStream_t st, const int32_t* row_keep, int keep_T) {
-  if (!x || !w || !logits || R < 1 || n_g < 1 || V < 1 || H < 8 || H % 8 != 0 || (row_keep && keep_T < 1))
+                             cudaStream_t st) {
+  if (!x || !w || !logits || R < 1 || n_g < 1 || V < 1 || H < 8 || H % 8 != 0)
     return MEDUSA_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(w) || !aligned16(logits)) return MEDUSA_ERR_ALIGNMENT;
   const VerifyPlan p = plan_tc(R, n_g, V);
@@ -1271,17 +1264,16 @@ int launch_group_logits_bf16(const void* x, int R, int n_g, const void* w, int H
                             : make_tmap_bf16_3d(&mx, x, H, n_g, R, static_cast<uint64_t>(H) * 2,
                                                 static_cast<uint64_t>(n_g) * H * 2, 1, p.qr);
   if (!okx || !make_tmap_bf16(&mw, w, static_cast<uint64_t>(n_g) * V, H, p.BN)) return MEDUSA_ERR_CUDA;
-  const EpiArgs ea{R, V, 1, 0, nullptr, medusa_tree_dev{}, 0.f, logits, nullptr, nullptr, nullptr, n_g, row_keep,
-                   keep_T};
+  const EpiArgs ea{R, V, 1, 0, nullptr, medusa_tree_dev{}, 0.f, logits, nullptr, nullptr, nullptr, n_g};
   return dispatch_tc(p, mx, mw, H, ea, st);
 }
 
 int group_topk_tiles(int R, int n_g, int V) { return plan_tc(R, n_g, V, true).n_nt; }
 
 int launch_group_topk_bf16(const void* x, int R, int n_g, const void* w, int H, int V, int k, float* cand_v,
-                           int* cand_i, float* logits, cudaStream_t st, const int32_t* row_keep, int keep_T) {
+                           int* cand_i, float* logits, cudaStream_t st) {
   if (!x || !w || !cand_v || !cand_i || R < 1 || n_g < 1 || V < 1 || H < 8 || H % 8 != 0 || k < 1 ||
-      k > kEpiTopkMax || (row_keep && keep_T < 1))
+      k > kEpiTopkMax)
     return MEDUSA_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(w) || (logits && !aligned16(logits))) return MEDUSA_ERR_ALIGNMENT;
   const VerifyPlan p = plan_tc(R, n_g, V, true);
@@ -1290,8 +1282,8 @@ int launch_group_topk_bf16(const void* x, int R, int n_g, const void* w, int H, 
                             : make_tmap_bf16_3d(&mx, x, H, n_g, R, static_cast<uint64_t>(H) * 2,
                                                 static_cast<uint64_t>(n_g) * H * 2, 1, p.qr);
   if (!okx || !make_tmap_bf16(&mw, w, static_cast<uint64_t>(n_g) * V, H, p.BN)) return MEDUSA_ERR_CUDA;
-  const EpiArgs ea{R,   V,        1,      p.n_nt, nullptr, medusa_tree_dev{}, 0.f, logits, nullptr, nullptr,
-                   nullptr, n_g, row_keep, keep_T, k,     cand_v,  cand_i};
+  const EpiArgs ea{R, V, 1, p.n_nt, nullptr, medusa_tree_dev{}, 0.f, logits, nullptr, nullptr, nullptr, n_g, k,
+                   cand_v, cand_i};
   return dispatch_tc(p, mx, mw, H, ea, st);
 }
 
@@ -1330,8 +1322,7 @@ MEDUSA_API int medusa_verify_accept(const medusa_tree* tree, const void* x, cons
   if (!ws || ws_bytes < w.bytes) return MEDUSA_ERR_WORKSPACE;
   auto st = reinterpret_cast<cudaStream_t>(stream);
   const float inv_tau = temperature > 0.f ? 1.f / temperature : 0.f;
-  EpiArgs ea{p.R, V, T, p.n_parts, tree_tokens, tree->dev, inv_tau, logits, w.part, w.child_z, dev_status, 1,
-             nullptr, 0};
+  EpiArgs ea{p.R, V, T, p.n_parts, tree_tokens, tree->dev, inv_tau, logits, w.part, w.child_z, dev_status, 1};
 
   if (dtype == MEDUSA_BF16) {
     CUtensorMap mx, mw;

@@ -75,7 +75,7 @@ class MedusaStep:
                              head_logits=self.head_logits, stream=stream)
 
     def heads_from_tree(self, X, W1, b1, W2, stream=None):
-        """Next step's candidates from the heads over every tree node's state X (the
+        """Next step's candidates from the heads on the tree nodes' states X (the
         verification input): the top-k of each request's accepted node go to
         ``topk_ids``/``topk_vals`` and its next token to ``root``, so the next
         :meth:`build` continues from the accepted branch."""

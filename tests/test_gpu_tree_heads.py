@@ -1,11 +1,13 @@
-"""GPU parity of the heads over every tree node (medusa_heads_topk_tree): the
-next step's candidates taken from the verification pass's hidden states.
+"""GPU parity of the heads on the tree nodes' hidden states
+(medusa_heads_topk_tree): the next step's candidates taken from the
+verification pass's hidden states.
 
 wiblog.cn "Medusa multi-head speculative decoding", section "Inference flow in
 an online chat service": the verification pass that scores the candidates also
 yields the next round's candidates, with no extra forward pass.  The kernels
-run the heads on all B*T rows (bf16: tensor-core GEMMs) and keep the top-k of
-each request's accepted row; the oracle runs the heads on that row alone.
+gather each request's accepted row and run the heads on those rows (bf16 from
+three requests: tensor-core GEMMs); the oracle runs the heads on the tree rows
+and keeps the accepted one.
 """
 import dataclasses
 
