@@ -41,10 +41,12 @@ template <int BMAX> struct Pass {
 };
 
 // Work split.  Both launches size their grid to the CTAs that are resident at
-// once (one wave) and split the weight rows evenly: first across CTAs, then
-// across the warps of a CTA, so no SM or warp carries a whole extra row group
-// at the end.  K2 gives every head (block) the same number of CTAs, so each
-// CTA's rows lie inside one head and its top-k candidates belong to that head.
+// once (one wave).  K1 splits the weight rows evenly: first across CTAs, then
+// across the warps of a CTA.  K2 gives every head (block) the same number of
+// CTAs, so each CTA's rows lie inside one head and its top-k candidates belong
+// to that head; with one or two activation rows and long heads it hands out a
+// block's rows dynamically (a counter every warp takes its next rows from),
+// else it splits them evenly like K1.
 struct HeadsPlan {
   bool tc;      // vocabulary projection on the tensor cores (bf16, >= kTcMinRows rows, root given)
   bool fused;   // tc, with the top-k in the GEMM epilogue (k <= 16, candidates fit the merge CTA)
@@ -125,6 +127,10 @@ bool plan_heads(int B, int H, int V, int K, int with_root, int esize, int topk, 
   return true;
 }
 
+// Self-resetting counters in the workspace: per block a merge ticket and the
+// row counter of K2's dynamic row split.
+inline size_t counter_ints(const HeadsPlan& p) { return 2 * static_cast<size_t>(p.nblk); }
+
 struct HeadsWs {
   void* u;
   float* z;    // [B, K, V] logits of the unfused tensor-core path when the caller keeps none
@@ -143,7 +149,7 @@ HeadsWs carve_heads_ws(void* base, const HeadsPlan& p, int B, int H, int V, int 
   auto take = [&](size_t n) { size_t s = o; o = align_up(o + n, 256); return s; };
   size_t ou = take(static_cast<size_t>(B) * K * H * esize);
   size_t ncand = p.fused ? 0 : static_cast<size_t>(p.nblk) * B * p.cph * topk;
-  size_t ov = take(ncand * 4), oi = take(ncand * 4), oc = take(static_cast<size_t>(p.nblk) * 4);
+  size_t ov = take(ncand * 4), oi = take(ncand * 4), oc = take(counter_ints(p) * 4);
   size_t oz = p.tc && !p.fused ? take(static_cast<size_t>(B) * K * V * 4) : 0;
   size_t ozf = p.tc ? take(static_cast<size_t>(B) * K * H * 4) : 0;
   const size_t ntc = p.fused ? static_cast<size_t>(B) * K * p.ntile * topk : 0;
@@ -171,6 +177,31 @@ __device__ inline void prefetch_rows(const T* W, long row0, long rows, int H) {
   if (lane * 128L >= row_bytes) return;
   for (long r = row0; r < row0 + kRows && r < row0 + rows; ++r)
     asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<const char*>(W + r * H) + lane * 128));
+}
+
+// K2 takes the dynamic split when every warp gets at least this many rows.
+constexpr int kDynMinRowsPerWarp = 16;
+
+// Rows a warp takes from a dynamic row split at a time (a multiple of R).
+template <int BMAX> struct Grab {
+  static constexpr int G = 4 * Pass<BMAX>::R;
+};
+
+// Next G rows of a dynamic split: lane 0 adds to the counter, the warp gets the
+// old value.  Issued one chunk ahead, so the atomic's round trip overlaps the
+// rows being processed.
+__device__ inline long grab_rows(int* ctr, int G) {
+  long r = 0;
+  if ((threadIdx.x & 31) == 0) r = atomicAdd(ctr, G);
+  return r;
+}
+
+// Ask L2 for whole weight rows [row0, row0 + n) (n <= 32, one bulk prefetch per lane).
+template <typename T>
+__device__ inline void prefetch_whole_rows(const T* W, long row0, int n, long nrows, int H) {
+  const int lane = threadIdx.x & 31;
+  if (lane < n && row0 + lane < nrows)
+    tc::prefetch_l2_bulk(W + (row0 + lane) * static_cast<long>(H), static_cast<uint32_t>(H * sizeof(T)));
 }
 
 // K1: rows [c*N/C, (c+1)*N/C) of W1 (flattened [K*H] rows) for CTA c, split
@@ -342,6 +373,156 @@ __global__ void __launch_bounds__(kThreads) heads_vocab_kernel(
   if (threadIdx.x == 0) counters[blk] = 0;  // ready for the next launch
 }
 
+// K2 for one or two activation rows: the rows of block blk (head blk's W2, or
+// lm_head for the root) in a dynamic split over the block's CTAs (every warp
+// takes the next G rows from the block's counter until none are left), so the
+// launch ends with little tail.  Each warp keeps the top-k of the rows it took,
+// per activation row, as a list spread over lanes 0..k-1 (value descending, equal
+// values by the lower id, NaN never taken): a row's logit enters if it beats the
+// k-th entry.  The CTA then merges its warps' lists into k candidates, and the
+// last CTA of the block (ticket) merges the CTAs' candidates, as in the static
+// split, and resets the block's counters.
+template <int BMAX>
+size_t vocab_dyn_smem_bytes(int nb, int H, int esize, int cph, int topk) {
+  return align_up(static_cast<size_t>(nb) * H * esize, 16) +
+         (2 * static_cast<size_t>(cph) * topk + 2 * kWarps * static_cast<size_t>(topk) + 2 * static_cast<size_t>(topk) +
+          2 * static_cast<size_t>(BMAX) * kWarps * topk) * 4;
+}
+
+template <typename T, int BMAX>
+__global__ void __launch_bounds__(kThreads, 2) heads_vocab_dyn_kernel(
+    const T* __restrict__ h, const T* __restrict__ u, const T* __restrict__ W2, const T* __restrict__ lm_head,
+    int B, int b0, int nb, int H, int V, int K, int topk, int cph, float* __restrict__ head_logits,
+    int32_t* __restrict__ topk_ids, float* __restrict__ topk_vals, int32_t* __restrict__ root_tok,
+    float* __restrict__ cand_v, int* __restrict__ cand_i, int* __restrict__ counters) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  const int nblk = gridDim.x / cph;
+  const int blk = blockIdx.x / cph, cta = blockIdx.x % cph;
+  const bool is_root = blk == K;
+  const int kk = is_root ? 1 : topk;
+  const T* W = is_root ? lm_head : W2 + static_cast<size_t>(blk) * V * H;
+  const T* x = is_root ? h + static_cast<size_t>(b0) * H : u + (static_cast<size_t>(b0) * K + blk) * H;
+  const size_t x_stride = is_root ? H : static_cast<size_t>(K) * H;
+  int* rowctr = counters + nblk + blk;
+
+  T* xs = reinterpret_cast<T*>(smem_raw);
+  float* mv = reinterpret_cast<float*>(smem_raw + align_up(static_cast<size_t>(nb) * H * sizeof(T), 16));
+  int* mi = reinterpret_cast<int*>(mv + static_cast<size_t>(cph) * topk);  // [cph * topk] merge
+  float* sv = reinterpret_cast<float*>(mi + static_cast<size_t>(cph) * topk);  // [kWarps * topk]
+  int* si = reinterpret_cast<int*>(sv + kWarps * topk);
+  float* fv = reinterpret_cast<float*>(si + kWarps * topk);  // [topk] final
+  int* fi = reinterpret_cast<int*>(fv + topk);
+  float* wv = reinterpret_cast<float*>(fi + topk);  // [BMAX][kWarps * topk] the warps' lists, kk apart
+  int* wi = reinterpret_cast<int*>(wv + BMAX * kWarps * topk);
+  __shared__ int s_last;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  constexpr int R = Pass<BMAX>::R, G = Grab<BMAX>::G;
+  // the block's counter was reset by this kernel's previous launch, which
+  // completed before any kernel ahead of this one did
+  long r0 = __shfl_sync(0xffffffffu, grab_rows(rowctr, G), 0);
+  prefetch_whole_rows(W, r0, G, V, H);
+  pdl_wait();
+  pdl_trigger();
+  stage_rows(xs, x, x_stride, nb, H);
+  __syncthreads();
+
+  float lv[BMAX], tv[BMAX];
+  int li[BMAX], ti[BMAX];
+#pragma unroll
+  for (int b = 0; b < BMAX; ++b) {
+    lv[b] = tv[b] = -INFINITY;
+    li[b] = ti[b] = 0x7fffffff;
+  }
+  while (r0 < V) {
+    const long nx = grab_rows(rowctr, G);
+    const int r1 = static_cast<int>(r0 + G < V ? r0 + G : V);
+    for (int row0 = static_cast<int>(r0); row0 < r1; row0 += R) {
+      const int valid = min(R, r1 - row0);
+      float acc[R][BMAX];
+      gemv_rows<T, BMAX, R, Pass<BMAX>::U>(W, static_cast<size_t>(row0), valid, H, xs, nb, acc);
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+#pragma unroll
+        for (int b = 0; b < BMAX; ++b) {
+          if (r < valid && b < nb) {
+            const float z = acc[r][b];  // every lane holds the row's logit
+            const int id = row0 + r;
+            if (head_logits && !is_root && lane == 0)
+              head_logits[(static_cast<size_t>(b0 + b) * K + blk) * V + id] = z;
+            if (better(z, id, tv[b], ti[b])) {
+              // fewer than kk entries are ahead of it: shift the rest down one lane
+              const int pos = __popc(__ballot_sync(0xffffffffu, lane < kk && better(lv[b], li[b], z, id)));
+              const float uv = __shfl_up_sync(0xffffffffu, lv[b], 1);
+              const int ui = __shfl_up_sync(0xffffffffu, li[b], 1);
+              if (lane == pos) {
+                lv[b] = z;
+                li[b] = id;
+              } else if (lane > pos && lane < kk) {
+                lv[b] = uv;
+                li[b] = ui;
+              }
+              tv[b] = __shfl_sync(0xffffffffu, lv[b], kk - 1);
+              ti[b] = __shfl_sync(0xffffffffu, li[b], kk - 1);
+            }
+          }
+        }
+      }
+    }
+    r0 = __shfl_sync(0xffffffffu, nx, 0);
+  }
+
+  // the warps' lists side by side (unfilled entries NaN, never taken), then one
+  // warp per activation row merges them into the CTA's candidates
+#pragma unroll
+  for (int b = 0; b < BMAX; ++b) {
+    if (b < nb && lane < kk) {
+      const bool filled = li[b] != 0x7fffffff;
+      wv[b * kWarps * topk + warp * kk + lane] = filled ? lv[b] : __int_as_float(0x7fc00000);
+      wi[b * kWarps * topk + warp * kk + lane] = filled ? li[b] : -1;
+    }
+  }
+  __syncthreads();
+  for (int b = warp; b < nb; b += kWarps) {
+    float* v = wv + b * kWarps * topk;
+    int* ids = wi + b * kWarps * topk;
+    const size_t cb = ((static_cast<size_t>(blk) * B + b0 + b) * cph + cta) * topk;
+    warp_topk_slice(v, ids, 0, kWarps * kk, kk, cand_v + cb, cand_i + cb, __int_as_float(0x7fc00000));
+  }
+
+  // the last CTA of this block merges every CTA's candidates
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) s_last = (atomicAdd(counters + blk, 1) == cph - 1);
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  for (int b = 0; b < nb; ++b) {
+    const size_t base = (static_cast<size_t>(blk) * B + b0 + b) * cph * topk;
+    const int m = cph * kk;
+    for (int e = threadIdx.x; e < m; e += blockDim.x) {
+      const int c = e / kk, t = e % kk;
+      mv[e] = __ldcg(cand_v + base + static_cast<size_t>(c) * topk + t);
+      mi[e] = __ldcg(cand_i + base + static_cast<size_t>(c) * topk + t);
+    }
+    __syncthreads();
+    block_topk(mv, mi, 0, m, kk, fv, fi, sv, si);
+    if (is_root) {
+      if (threadIdx.x == 0) root_tok[b0 + b] = fi[0];
+    } else {
+      for (int t = threadIdx.x; t < topk; t += blockDim.x) {
+        topk_ids[(static_cast<size_t>(b0 + b) * K + blk) * topk + t] = fi[t];
+        topk_vals[(static_cast<size_t>(b0 + b) * K + blk) * topk + t] = fv[t];
+      }
+    }
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {  // ready for the next launch
+    counters[blk] = 0;
+    *rowctr = 0;
+  }
+}
+
 template <typename T, int BMAX>
 int launch_fc(const HeadsPlan& p, const HeadsWs& w, const T* h, const T* W1, const T* b1, int b0, int nb, int H,
               int K, cudaStream_t st) {
@@ -362,6 +543,23 @@ template <typename T, int BMAX, bool FROMZ>
 int launch_vocab(const HeadsPlan& p, const HeadsWs& w, const T* h, const T* W2, const T* lm, int B, int b0, int nb,
                  int H, int V, int K, int topk, float* head_logits, int32_t* topk_ids, float* topk_vals,
                  int32_t* root_tok, const float* zsrc, cudaStream_t st) {
+  if constexpr (!FROMZ && BMAX <= 2) {
+    // short heads keep the static split: the counter's round trips would cost more than the tail
+    if (static_cast<long>(V) >= static_cast<long>(kDynMinRowsPerWarp) * p.cph * kWarps) {
+      const size_t smem = vocab_dyn_smem_bytes<BMAX>(nb, H, sizeof(T), p.cph, topk);
+      auto vk = heads_vocab_dyn_kernel<T, BMAX>;
+      if (!ensure_dyn_smem(vk, smem))
+        return MEDUSA_ERR_CUDA;
+      if (launch_pdl(vk, dim3(p.nblk * p.cph), dim3(kThreads), smem, st, h, static_cast<const T*>(w.u), W2, lm, B,
+                     b0, nb, H, V, K, topk, p.cph, head_logits, topk_ids, topk_vals, root_tok, w.cand_v, w.cand_i,
+                     w.counters) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return MEDUSA_ERR_CUDA;
+      }
+      MEDUSA_LAUNCH_CHECK();
+      return MEDUSA_OK;
+    }
+  }
   const size_t smem = vocab_smem_bytes(nb, BMAX, H, sizeof(T), p.rpc, p.cph, topk);
   auto vk = heads_vocab_kernel<T, BMAX, FROMZ>;
   if (!ensure_dyn_smem(vk, smem))
@@ -710,7 +908,7 @@ MEDUSA_API int medusa_heads_topk_noalloc(const void* h, const void* w1, const vo
   if (rc != MEDUSA_OK) return rc;
   HeadsWs w = carve_heads_ws(scratch, p, B, H, V, K, topk, es);
   // the ticket counters must start at zero whatever an earlier call left behind
-  if (cudaMemsetAsync(w.counters, 0, static_cast<size_t>(p.nblk) * sizeof(int), st) != cudaSuccess) {
+  if (cudaMemsetAsync(w.counters, 0, counter_ints(p) * sizeof(int), st) != cudaSuccess) {
     (void)cudaGetLastError();
     return MEDUSA_ERR_CUDA;
   }

@@ -126,11 +126,15 @@ def test_tiny_full_step(mb, variant, temperature, near_ties):
         assert int(step.accept_len[0]) == 2
 
 
-def test_tiny_root_from_lm_head(mb, near_ties):
-    wl = synth.WORKLOADS["tiny"]
+@pytest.mark.parametrize("name", ["tiny", "vicuna7b"])
+def test_root_from_lm_head(mb, name, near_ties):
+    """The root as argmax lm_head(h), an extra block of the vocabulary launch: at the 7B
+    shape that launch hands its rows out dynamically, at the tiny one it splits them
+    statically."""
+    wl = synth.WORKLOADS[name]
     inp = synth.make_inputs(wl, "cuda")
     step, kc, vc, kl = run_step(mb, wl, inp, 0.7, root_from_lm=True)
-    near_ties(check_full(wl, inp, step, kc, vc, kl, 0.7, root_from_lm=True))
+    assert near_ties(check_full(wl, inp, step, kc, vc, kl, 0.7, root_from_lm=True)) <= 2
 
 
 @pytest.mark.parametrize("name", ["tiny", "vicuna7b"])
