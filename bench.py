@@ -453,7 +453,7 @@ def run_ours(args, ws, rank, local):
     roof = None
     if heads_ms:
         ach = sb["heads"] / (heads_ms / 1e3) / 1e9
-        roof = {"kernel": "medusa_heads_topk (heads_fc + heads_vocab_topk)", "bound": "hbm",
+        roof = {"kernel": "medusa_heads_topk (the heads stage: W1 and W2 streams with the top-k)", "bound": "hbm",
                 "achieved": round(ach, 1), "peak": hbm, "unit": "GB/s", "frac": round(ach / hbm, 4),
                 "peak_source": src, "algorithmic_bytes": sb["heads"],
                 "traffic": traffic_from_profile("heads_vicuna7b") if wl.name == "vicuna7b" else None}
