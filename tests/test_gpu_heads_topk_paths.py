@@ -82,3 +82,37 @@ def test_batched_heads_nan_row_gets_no_candidate(mb, topk):
     assert (ids[2] == -1).all() and torch.isneginf(vals[2]).all()
     keep = [0, 1, 3]
     assert torch.equal(ids[keep], clean_ids[keep]) and torch.equal(vals[keep], clean_vals[keep])
+
+
+@pytest.mark.parametrize("with_lm", [False, True])
+@pytest.mark.parametrize("B", [1, 2])
+def test_vocabulary_stream_dynamic_split(mb, B, with_lm, near_ties):
+    """One or two activation rows on a vocabulary long enough for the dynamic row split
+    (at least 16 rows per warp) and not a multiple of the 4 rows a warp takes at a time,
+    with and without the lm_head root block: top-k, head logits and root against the
+    oracle."""
+    wl = dataclasses.replace(SMALL_BF16, name="heads_dyn", config_id=78, V=7557, B=B, K=5)
+    inp = synth.make_inputs(wl, "cuda")
+    k = 10
+    ws = mb.workspace(mb.medusa_heads_topk_workspace_size(B, wl.H, wl.V, wl.K, k, int(with_lm), mb.MEDUSA_BF16),
+                      "cuda")
+    ids = torch.full((B, wl.K, k), -3, dtype=torch.int32, device="cuda")
+    vals = torch.zeros(B, wl.K, k, device="cuda")
+    root = torch.full((B,), -3, dtype=torch.int32, device="cuda")
+    logits = torch.zeros(B, wl.K, wl.V, device="cuda")
+    for _ in range(2):   # the counters reset themselves
+        mb.medusa_heads_topk(inp.h, inp.W1, inp.b1, inp.W2, inp.lm_head if with_lm else None, k, ids, vals, root,
+                             ws, head_logits=logits)
+    torch.cuda.synchronize()
+    z_o = oracle_logits(inp, wl)
+    assert rel_err(logits, z_o) < TOL["bf16"]
+    near = check_topk(ids, vals, z_o, k, DELTA["bf16"])
+    if with_lm:
+        h, lm = _f64(inp.h), _f64(inp.lm_head)
+        z_root = h @ lm.T
+        for b in range(B):
+            g, r = int(root[b]), int(oracle.base_root(h[b:b + 1], lm)[0])
+            if g != r:
+                assert abs(z_root[b, g] - z_root[b, r]) < DELTA["bf16"] * max(1.0, abs(z_root[b, r]))
+                near += 1
+    assert near_ties(near) <= 3
