@@ -236,11 +236,11 @@ def run_ours(args, ws, rank, local):
         step.attention(inp.q, inp.k_new, inp.v_new, kc, vc, kl)
         if timed_events:
             e[2].record()
-        step.verify(inp.X, inp.lm_head, tau, wl.posterior_threshold, wl.posterior_alpha)
+        # verification, acceptance and the KV commit of the winner (one launch sequence)
+        step.verify_commit(inp.X, inp.lm_head, inp.k_new, inp.v_new, kc, vc, kl, tau, wl.posterior_threshold,
+                           wl.posterior_alpha)
         if timed_events:
             e[3].record()
-        step.commit(inp.k_new, inp.v_new, kc, vc, kl)
-        if timed_events:
             e[4].record()
             ev_pairs.append(e)
 
@@ -325,8 +325,8 @@ def run_ours(args, ws, rank, local):
         kl.copy_(kv_len0)
         step.build(kl)
         step.attention(inp.q, inp.k_new, inp.v_new, kc, vc, kl)
-        step.verify(inp.X, inp.lm_head, tau, wl.posterior_threshold, wl.posterior_alpha)
-        step.commit(inp.k_new, inp.v_new, kc, vc, kl)
+        step.verify_commit(inp.X, inp.lm_head, inp.k_new, inp.v_new, kc, vc, kl, tau, wl.posterior_threshold,
+                           wl.posterior_alpha)
         step.heads_from_tree(inp.X, inp.W1, inp.b1, inp.W2)
     with torch.cuda.stream(s):
         steady_step()                       # workspace of the tree heads, kernel attributes

@@ -322,6 +322,27 @@ int medusa_verify_accept(const medusa_tree* tree, const void* x, const void* lm_
                          void* ws, size_t ws_bytes, medusa_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * medusa_verify_accept_commit
+ * medusa_verify_accept followed by medusa_kv_commit of its winner, with one
+ * launch fewer: the CTA that runs a request's acceptance also copies the
+ * accepted path's K/V rows (depth 0..accept_len) from k_new/v_new into the
+ * cache at kv_len.. and advances kv_len, with medusa_kv_commit's rules (a
+ * request whose rows would pass Lmax is flagged MEDUSA_DEV_KV_OVERFLOW and
+ * left untouched).  Arguments as the two calls; k_new, v_new [B,T,Hkv,D] and
+ * the cache [B,Hkv,Lmax,D] in `dtype`; (D * element size) % 16 == 0.  The
+ * workspace is medusa_verify_accept's.
+ * ---------------------------------------------------------------------- */
+int medusa_verify_accept_commit(const medusa_tree* tree, const void* x, const void* lm_head,
+                                const int32_t* tree_tokens, int32_t B, int32_t H, int32_t V,
+                                medusa_dtype dtype, float temperature, float posterior_threshold,
+                                float posterior_alpha, int32_t tie_break, float* logits, float* node_p,
+                                float* node_H, int32_t* accept_len, int32_t* best_path, int32_t* best_node,
+                                int32_t* accepted_tokens, int32_t* next_root, int32_t* dev_status,
+                                const void* k_new, const void* v_new, void* k_cache, void* v_cache,
+                                int32_t* kv_len, int32_t Hkv, int32_t D, int32_t Lmax, void* ws,
+                                size_t ws_bytes, medusa_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * medusa_sample_next
  * The next token drawn from the top-p nucleus of the accepted node's
  * distribution softmax(z[best_node] / temperature), instead of its greedy

@@ -82,6 +82,9 @@ _sig("medusa_verify_accept", ctypes.c_int,
      [_vp, _vp, _vp, _vp, _i32, _i32, _i32, ctypes.c_int, _f32, _f32, _f32, _i32, _vp, _vp, _vp, _vp, _vp, _vp,
       _vp, _vp, _vp, _vp, _sz, _vp])
 _sig("medusa_sample_next", ctypes.c_int, [_vp, _vp, _vp, _vp, _i32, _i32, _f32, _f32, _vp, _vp])
+_sig("medusa_verify_accept_commit", ctypes.c_int,
+     [_vp, _vp, _vp, _vp, _i32, _i32, _i32, ctypes.c_int, _f32, _f32, _f32, _i32, _vp, _vp, _vp, _vp, _vp, _vp,
+      _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _vp, _sz, _vp])
 _sig("medusa_kv_commit", ctypes.c_int,
      [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, ctypes.c_int, _vp, _vp])
 
@@ -250,6 +253,23 @@ def medusa_verify_accept(tree: Tree, x, lm_head, tree_tokens, temperature: float
         posterior_threshold, posterior_alpha, tb, _ptr(logits), _ptr(node_p), _ptr(node_H), _ptr(accept_len),
         _ptr(best_path), _ptr(best_node), _ptr(accepted_tokens), _ptr(next_root), _ptr(dev_status), _ptr(ws),
         ws.numel(), _stream(stream)))
+
+
+def medusa_verify_accept_commit(tree: Tree, x, lm_head, tree_tokens, temperature: float, posterior_threshold: float,
+                                posterior_alpha: float, accept_len, best_path, best_node, accepted_tokens, next_root,
+                                k_new, v_new, k_cache, v_cache, kv_len, ws, logits=None, node_p=None, node_H=None,
+                                dev_status=None, stream=None, tie_break: str = "first") -> None:
+    """medusa_verify_accept and the KV commit of its winner in one launch sequence."""
+    B, T, H = x.shape
+    V = lm_head.shape[0]
+    _, Hkv, Lmax, D = k_cache.shape
+    tb = {"first": 0, "joint": 1}[tie_break]
+    _check("medusa_verify_accept_commit", lib.medusa_verify_accept_commit(
+        tree.handle, _ptr(x), _ptr(lm_head), _ptr(tree_tokens), B, H, V, dtype_code(x), temperature,
+        posterior_threshold, posterior_alpha, tb, _ptr(logits), _ptr(node_p), _ptr(node_H), _ptr(accept_len),
+        _ptr(best_path), _ptr(best_node), _ptr(accepted_tokens), _ptr(next_root), _ptr(dev_status), _ptr(k_new),
+        _ptr(v_new), _ptr(k_cache), _ptr(v_cache), _ptr(kv_len), Hkv, D, Lmax, _ptr(ws), ws.numel(),
+        _stream(stream)))
 
 
 def medusa_kv_commit(tree: Tree, k_new, v_new, k_cache, v_cache, kv_len, best_node, dev_status=None,

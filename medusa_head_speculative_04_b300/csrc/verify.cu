@@ -821,6 +821,13 @@ struct AcceptArgs {
   int32_t* accepted_tokens;
   int32_t* next_root;
   int32_t* dev_status;
+  // the KV commit of the accepted path, run by the same CTA (k_cache NULL: none)
+  const uint4* k_new;
+  const uint4* v_new;
+  uint4* k_cache;
+  uint4* v_cache;
+  int32_t* kv_len;
+  int Hkv, row_vecs, Lmax;
 };
 
 // ------------------------------------------------------------------------
@@ -883,6 +890,48 @@ __device__ void accept_request(const AcceptArgs& a, int b, unsigned char* s_acc,
     a.accept_len[b] = a_len;
     a.best_node[b] = best;
     a.best_path[b] = s_fp[best];
+  }
+  if (a.k_cache) {
+    // the commit (what medusa_kv_commit does): the path's K/V rows root..best go to
+    // cache positions kv_len..kv_len+a_len, then kv_len advances; a request whose
+    // rows would pass Lmax is flagged and its cache left untouched
+    __shared__ int s_L;
+    if (threadIdx.x == 0) {
+      const int L = a.kv_len[b];
+      s_L = (L < 0 || L + a_len + 1 > a.Lmax) ? -1 : L;
+      if (s_L < 0 && a.dev_status) atomicOr(a.dev_status + b, MEDUSA_DEV_KV_OVERFLOW);
+    }
+    __syncthreads();
+    const int L = s_L;
+    if (L >= 0) {
+      const int per_d = a.Hkv * a.row_vecs, total = (a_len + 1) * per_d;
+      constexpr int U = 4;  // all loads of a round before its stores
+      for (int e0 = threadIdx.x; e0 < total; e0 += blockDim.x * U) {
+        uint4 kr[U], vr[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const int e = e0 + u * blockDim.x;
+          if (e < total) {
+            const int d = e / per_d, g = (e / a.row_vecs) % a.Hkv, j = e % a.row_vecs;
+            const size_t src = ((base + s_chain[d]) * a.Hkv + g) * a.row_vecs + j;
+            kr[u] = a.k_new[src];
+            vr[u] = a.v_new[src];
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const int e = e0 + u * blockDim.x;
+          if (e < total) {
+            const int d = e / per_d, g = (e / a.row_vecs) % a.Hkv, j = e % a.row_vecs;
+            const size_t dst = ((static_cast<size_t>(b) * a.Hkv + g) * a.Lmax + L + d) * a.row_vecs + j;
+            a.k_cache[dst] = kr[u];
+            a.v_cache[dst] = vr[u];
+          }
+        }
+      }
+      __syncthreads();
+      if (threadIdx.x == 0) a.kv_len[b] = L + a_len + 1;
+    }
   }
   __syncthreads();
 }
@@ -1296,13 +1345,23 @@ MEDUSA_API size_t medusa_verify_accept_workspace_size(const medusa_tree* tree, i
   return carve_verify_ws(nullptr, p, V, dtype).bytes;
 }
 
-MEDUSA_API int medusa_verify_accept(const medusa_tree* tree, const void* x, const void* lm_head,
-                                    const int32_t* tree_tokens, int32_t B, int32_t H, int32_t V, medusa_dtype dtype,
-                                    float temperature, float posterior_threshold, float posterior_alpha,
-                                    int32_t tie_break, float* logits, float* node_p, float* node_H, int32_t* accept_len,
-                                    int32_t* best_path, int32_t* best_node, int32_t* accepted_tokens,
-                                    int32_t* next_root, int32_t* dev_status, void* ws, size_t ws_bytes,
-                                    medusa_stream_t stream) {
+namespace {
+
+struct CommitArgs {
+  const void* k_new;
+  const void* v_new;
+  void* k_cache;
+  void* v_cache;
+  int32_t* kv_len;
+  int Hkv, D, Lmax;
+};
+
+int verify_accept_impl(const medusa_tree* tree, const void* x, const void* lm_head, const int32_t* tree_tokens,
+                       int32_t B, int32_t H, int32_t V, medusa_dtype dtype, float temperature,
+                       float posterior_threshold, float posterior_alpha, int32_t tie_break, float* logits,
+                       float* node_p, float* node_H, int32_t* accept_len, int32_t* best_path, int32_t* best_node,
+                       int32_t* accepted_tokens, int32_t* next_root, int32_t* dev_status, void* ws, size_t ws_bytes,
+                       medusa_stream_t stream, const CommitArgs* cm) {
   if (!tree || !x || !lm_head || !tree_tokens || !accept_len || !best_path || !best_node || !accepted_tokens ||
       !next_root)
     return MEDUSA_ERR_INVALID_ARG;
@@ -1361,6 +1420,17 @@ MEDUSA_API int medusa_verify_accept(const medusa_tree* tree, const void* x, cons
   AcceptArgs aa{tree->dev, tree_tokens, w.part, p.n_parts, p.R, w.rowst, w.acc, w.logp, tie_break, w.tickets,
                 w.child_z, inv_tau, posterior_threshold, posterior_alpha, node_p, node_H, accept_len, best_path,
                 best_node, accepted_tokens, next_root, dev_status};
+  if (cm) {
+    const int es = dtype == MEDUSA_BF16 ? 2 : 4;
+    aa.k_new = static_cast<const uint4*>(cm->k_new);
+    aa.v_new = static_cast<const uint4*>(cm->v_new);
+    aa.k_cache = static_cast<uint4*>(cm->k_cache);
+    aa.v_cache = static_cast<uint4*>(cm->v_cache);
+    aa.kv_len = cm->kv_len;
+    aa.Hkv = cm->Hkv;
+    aa.row_vecs = cm->D * es / 16;
+    aa.Lmax = cm->Lmax;
+  }
   const size_t accept_smem = static_cast<size_t>(T) * 6 + (T & 1) * 2 + static_cast<size_t>(T) * 5;
   if (launch_pdl(merge_accept_kernel, dim3(cdiv(p.R, kMergeRows)), dim3(kMergeRows * 32), accept_smem, st, aa) !=
       cudaSuccess) {
@@ -1369,4 +1439,40 @@ MEDUSA_API int medusa_verify_accept(const medusa_tree* tree, const void* x, cons
   }
   MEDUSA_LAUNCH_CHECK();
   return MEDUSA_OK;
+}
+
+}  // namespace
+
+MEDUSA_API int medusa_verify_accept(const medusa_tree* tree, const void* x, const void* lm_head,
+                                    const int32_t* tree_tokens, int32_t B, int32_t H, int32_t V, medusa_dtype dtype,
+                                    float temperature, float posterior_threshold, float posterior_alpha,
+                                    int32_t tie_break, float* logits, float* node_p, float* node_H, int32_t* accept_len,
+                                    int32_t* best_path, int32_t* best_node, int32_t* accepted_tokens,
+                                    int32_t* next_root, int32_t* dev_status, void* ws, size_t ws_bytes,
+                                    medusa_stream_t stream) {
+  return verify_accept_impl(tree, x, lm_head, tree_tokens, B, H, V, dtype, temperature, posterior_threshold,
+                            posterior_alpha, tie_break, logits, node_p, node_H, accept_len, best_path, best_node,
+                            accepted_tokens, next_root, dev_status, ws, ws_bytes, stream, nullptr);
+}
+
+MEDUSA_API int medusa_verify_accept_commit(const medusa_tree* tree, const void* x, const void* lm_head,
+                                           const int32_t* tree_tokens, int32_t B, int32_t H, int32_t V,
+                                           medusa_dtype dtype, float temperature, float posterior_threshold,
+                                           float posterior_alpha, int32_t tie_break, float* logits, float* node_p,
+                                           float* node_H, int32_t* accept_len, int32_t* best_path,
+                                           int32_t* best_node, int32_t* accepted_tokens, int32_t* next_root,
+                                           int32_t* dev_status, const void* k_new, const void* v_new, void* k_cache,
+                                           void* v_cache, int32_t* kv_len, int32_t Hkv, int32_t D, int32_t Lmax,
+                                           void* ws, size_t ws_bytes, medusa_stream_t stream) {
+  if (!k_new || !v_new || !k_cache || !v_cache || !kv_len) return MEDUSA_ERR_INVALID_ARG;
+  if (Hkv < 1 || D < 1 || Lmax < 0) return MEDUSA_ERR_INVALID_ARG;
+  const int es = dtype == MEDUSA_BF16 ? 2 : 4;
+  if ((D * es) % 16 != 0) return MEDUSA_ERR_UNSUPPORTED;
+  const void* ptrs[] = {k_new, v_new, k_cache, v_cache, kv_len};
+  for (const void* q : ptrs)
+    if (!aligned16(q)) return MEDUSA_ERR_ALIGNMENT;
+  const CommitArgs cm{k_new, v_new, k_cache, v_cache, kv_len, Hkv, D, Lmax};
+  return verify_accept_impl(tree, x, lm_head, tree_tokens, B, H, V, dtype, temperature, posterior_threshold,
+                            posterior_alpha, tie_break, logits, node_p, node_H, accept_len, best_path, best_node,
+                            accepted_tokens, next_root, dev_status, ws, ws_bytes, stream, &cm);
 }

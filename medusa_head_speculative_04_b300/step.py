@@ -104,6 +104,17 @@ class MedusaStep:
                                 node_H=self.node_H, dev_status=self.dev_status, stream=stream,
                                 tie_break=self.tie_break)
 
+    def verify_commit(self, X, lm_head, k_new, v_new, k_cache, v_cache, kv_len, temperature: float,
+                      threshold: float = 0.09, alpha: float = 0.3, stream=None):
+        """:meth:`verify` and :meth:`commit` with one launch fewer (the acceptance's CTA
+        of a request also commits its accepted rows)."""
+        mb.medusa_verify_accept_commit(self.tree, X, lm_head, self.tokens, temperature, threshold, alpha,
+                                       self.accept_len, self.best_path, self.best_node, self.accepted_tokens,
+                                       self.next_root, self.k_rot if self.rope else k_new, v_new, k_cache, v_cache,
+                                       kv_len, self.ws_verify, logits=self.logits, node_p=self.node_p,
+                                       node_H=self.node_H, dev_status=self.dev_status, stream=stream,
+                                       tie_break=self.tie_break)
+
     def commit(self, k_new, v_new, k_cache, v_cache, kv_len, stream=None):
         mb.medusa_kv_commit(self.tree, self.k_rot if self.rope else k_new, v_new, k_cache, v_cache, kv_len,
                             self.best_node,
@@ -118,8 +129,8 @@ class MedusaStep:
         self.heads(h, W1, b1, W2, lm_head, stream=stream)
         self.build(kv_len, stream=stream)
         self.attention(q, k_new, v_new, k_cache, v_cache, kv_len, stream=stream)
-        self.verify(X, lm_head, temperature, threshold, alpha, stream=stream)
-        self.commit(k_new, v_new, k_cache, v_cache, kv_len, stream=stream)
+        self.verify_commit(X, lm_head, k_new, v_new, k_cache, v_cache, kv_len, temperature, threshold, alpha,
+                           stream=stream)
 
     def capture(self, *args, prologue=None, epilogue=None, stream: Optional[torch.cuda.Stream] = None, **kwargs):
         """Capture one whole step (the arguments of :meth:`run`) in a CUDA graph.

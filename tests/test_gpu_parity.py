@@ -384,3 +384,37 @@ def test_joint_tie_break_step(mb, wl, temperature, near_ties):
     step, kc, vc, kl = run_step(mb, wl, inp, temperature, tie_break="joint")
     near = near_ties(check_full(wl, inp, step, kc, vc, kl, temperature, tie_break="joint"))
     assert near <= 3
+
+
+@pytest.mark.parametrize("name", ["tiny", "small_bf16"])
+def test_fused_commit_matches_separate_calls(mb, name):
+    """medusa_verify_accept_commit (the commit run by the acceptance's CTA) leaves the same
+    results, cache, kv_len and status as medusa_verify_accept followed by medusa_kv_commit,
+    including a request whose accepted rows would pass Lmax (flagged, cache untouched)."""
+    wl = SMALL_BF16 if name == "small_bf16" else synth.WORKLOADS[name]
+    inp = synth.make_inputs(wl, "cuda", variant="plant")
+    kl_start = inp.kv_len.clone()
+    kl_start[0] = wl.Lmax              # request 0 cannot take even its root row
+    outs = []
+    for fused in (False, True):
+        step = make_step(mb, wl, inp)
+        kc, vc, kl = inp.k_cache.clone(), inp.v_cache.clone(), kl_start.clone()
+        step.root.copy_(inp.root)
+        step.heads(inp.h, inp.W1, inp.b1, inp.W2)
+        step.build(kl)
+        step.attention(inp.q, inp.k_new, inp.v_new, kc, vc, kl)
+        if fused:
+            step.verify_commit(inp.X, inp.lm_head, inp.k_new, inp.v_new, kc, vc, kl, 0.7, wl.posterior_threshold,
+                               wl.posterior_alpha)
+        else:
+            step.verify(inp.X, inp.lm_head, 0.7, wl.posterior_threshold, wl.posterior_alpha)
+            step.commit(inp.k_new, inp.v_new, kc, vc, kl)
+        torch.cuda.synchronize()
+        outs.append((step.results.clone(), step.dev_status.clone(), kc, vc, kl))
+    (r0, s0, kc0, vc0, kl0), (r1, s1, kc1, vc1, kl1) = outs
+    assert torch.equal(r0, r1) and torch.equal(s0, s1)
+    assert torch.equal(kl0, kl1) and torch.equal(kc0, kc1) and torch.equal(vc0, vc1)
+    assert int(s1[0]) & mb.DEV_KV_OVERFLOW and int(kl1[0]) == wl.Lmax
+    assert torch.equal(kc1[0], inp.k_cache[0])
+    if wl.B > 1:
+        assert all(int(kl1[b]) > int(kl_start[b]) for b in range(1, wl.B))
