@@ -118,3 +118,15 @@ def test_heads_workspace_holds_the_tensor_core_buffers(lib):
     assert 0 < f(B, H, V, K, topk, 1, 1) < base
     assert 0 < f(B, H, V, K, topk, 0, 0) < base
     assert 0 < f(2, H, V, K, topk, 0, 1) < base
+
+
+def test_verify_accept_commit_host_validation(lib):
+    """The fused acceptance + commit call rejects missing commit buffers on the host,
+    before anything is launched (no tree is needed to get that far)."""
+    f = lib.lib.medusa_verify_accept_commit
+    buf = ctypes.create_string_buffer(64)
+    p = ctypes.addressof(buf)
+    # no k_new: invalid before any launch
+    rc = f(None, p, p, p, 1, 4096, 32000, 1, 0.7, 0.09, 0.3, 0, None, None, None, p, p, p, p, p, None,
+           None, p, p, p, p, 32, 128, 2112, p, 1 << 20, None)
+    assert rc == -1
